@@ -1,0 +1,309 @@
+// fa_api.cu -- the C ABI of libfa.so (declared in include/fa.h): argument
+// validation, TMA descriptor encoding, kernel dispatch and the device status
+// word.  No compute happens here; every step of the path runs in the kernels
+// of fa_fwd_sm103.cu, fa_fwd_f32.cu and fa_bwd_sm103.cu.
+#include <climits>
+#include <cmath>
+#include <cstdlib>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_internal.h"
+
+namespace fa {
+
+// ------------------------------------------------------------ driver glue
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+constexpr int kMaxDevices = 64;
+
+}  // namespace
+
+int encode_tmap_3d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes, uint64_t inner,
+                   uint64_t rows, uint64_t planes, uint32_t box_inner, uint32_t box_rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return ERR_CUDA;
+    const cuuint64_t dims[3] = {inner, rows, planes};
+    const cuuint64_t strides[2] = {inner * (uint64_t)elem_bytes, rows * inner * (uint64_t)elem_bytes};
+    const cuuint32_t box[3] = {box_inner, box_rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(map, dtype, 3, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? OK : ERR_CUDA;
+}
+
+int device_sm_count()
+{
+    static int cache[kMaxDevices] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return 1;
+    if (dev >= 0 && dev < kMaxDevices && cache[dev] > 0)
+        return cache[dev];
+    int n = 1;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (dev >= 0 && dev < kMaxDevices)
+        cache[dev] = n;
+    return n;
+}
+
+uint64_t wait_timeout_ns()
+{
+    static const uint64_t ns = [] {
+        const char *e = std::getenv("FA_WAIT_TIMEOUT_MS");
+        long ms = e ? std::strtol(e, nullptr, 10) : 0;
+        if (ms <= 0)
+            ms = 4000;
+        return (uint64_t)ms * 1000000ull;
+    }();
+    return ns;
+}
+
+// ------------------------------------------------------------ fill kernel
+// Rows with no key at all (Tk == 0): O = 0, lse = -inf.
+__global__ void fill_empty_kernel(uint8_t *o, float *lse, size_t rows, int row_bytes)
+{
+    const size_t n16 = rows * (size_t)(row_bytes / 16);
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n16; i += (size_t)gridDim.x * blockDim.x)
+        reinterpret_cast<uint4 *>(o)[i] = make_uint4(0, 0, 0, 0);
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < rows; i += (size_t)gridDim.x * blockDim.x)
+        lse[i] = -INFINITY;
+}
+
+int fill_empty_launch(void *o, float *lse, size_t rows, int d, int elem_bytes, cudaStream_t s)
+{
+    const int grid = device_sm_count() * 4;
+    fill_empty_kernel<<<grid, 256, 0, s>>>(static_cast<uint8_t *>(o), lse, rows, d * elem_bytes);
+    return cudaGetLastError() == cudaSuccess ? OK : ERR_CUDA;
+}
+
+// ------------------------------------------------------------ validation
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb)
+{
+    if (!a || !b || na == 0 || nb == 0)
+        return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + nb && b0 < a0 + na;
+}
+
+// sm_103 check of the current device (cached).
+int check_device()
+{
+    static int cache[kMaxDevices] = {0};   // 0 unknown, 1 ok, 2 unsupported
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return ERR_CUDA;
+    if (dev >= 0 && dev < kMaxDevices && cache[dev])
+        return cache[dev] == 1 ? OK : ERR_UNSUPPORTED;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return ERR_CUDA;
+    const bool ok = (major == 10 && minor == 3);
+    if (dev >= 0 && dev < kMaxDevices)
+        cache[dev] = ok ? 1 : 2;
+    return ok ? OK : ERR_UNSUPPORTED;
+}
+
+// Shapes, flags and scale shared by every entry point.
+int check_sizes(int B, int H, int Tq, int Tk, int d, int causal, float scale)
+{
+    if (B < 0 || H < 0 || Tq < 0 || Tk < 0)
+        return ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1)
+        return ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.0f))
+        return ERR_INVALID_ARG;
+    if (d != 64 && d != 128 && d != 256)
+        return ERR_UNSUPPORTED;
+    // every (b*H + h) * T + row index must fit in 32 bits
+    const long long bh = (long long)B * H;
+    if (bh * (long long)(Tq > Tk ? Tq : Tk) > INT_MAX)
+        return ERR_INVALID_ARG;
+    return OK;
+}
+
+int check_fwd(const void *q, const void *k, const void *v, const void *o, const float *lse, int B, int H,
+              int Tq, int Tk, int d, int causal, float scale, int elem)
+{
+    int st = check_sizes(B, H, Tq, Tk, d, causal, scale);
+    if (st != OK)
+        return st;
+    const size_t bh = (size_t)B * H;
+    if (bh * Tq == 0)
+        return OK;
+    const size_t nq = bh * Tq * d * elem, nk = bh * Tk * d * elem, nl = bh * Tq * sizeof(float);
+    if (!q || !o || !lse || (Tk > 0 && (!k || !v)))
+        return ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return ERR_INVALID_ARG;
+    if (overlaps(o, nq, q, nq) || overlaps(o, nq, k, nk) || overlaps(o, nq, v, nk) || overlaps(o, nq, lse, nl) ||
+        overlaps(lse, nl, q, nq) || overlaps(lse, nl, k, nk) || overlaps(lse, nl, v, nk))
+        return ERR_INVALID_ARG;
+    return check_device();
+}
+
+size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace
+
+size_t bwd_row_stride(int Tq) { return ((size_t)Tq + 127) / 128 * 128; }
+
+size_t bwd_workspace_bytes(int BH, int Tq, int d)
+{
+    const size_t rows = (size_t)BH * bwd_row_stride(Tq);
+    return 2 * round256(rows * sizeof(float)) + round256(rows * d * sizeof(float));
+}
+
+BwdWorkspace bwd_workspace_carve(void *ws, int BH, int Tq, int d)
+{
+    const size_t rows = (size_t)BH * bwd_row_stride(Tq);
+    uint8_t *p = static_cast<uint8_t *>(ws);
+    BwdWorkspace w;
+    w.lse2 = reinterpret_cast<float *>(p);
+    w.delta = reinterpret_cast<float *>(p + round256(rows * sizeof(float)));
+    w.dq_acc = reinterpret_cast<float *>(p + 2 * round256(rows * sizeof(float)));
+    (void)d;
+    return w;
+}
+
+}  // namespace fa
+
+// ================================================================ C ABI
+extern "C" {
+
+int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Tq, int Tk, int d,
+           int causal, float scale, fa_stream_t stream)
+{
+    int st = fa::check_fwd(q, k, v, o, lse, B, H, Tq, Tk, d, causal, scale, 2);
+    if (st != fa::OK)
+        return st;
+    const int BH = B * H;
+    if ((size_t)BH * Tq == 0)
+        return FA_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (Tk == 0)
+        return fa::fill_empty_launch(o, lse, (size_t)BH * Tq, d, 2, s);
+    return fa::fwd_bf16_launch(q, k, v, o, lse, BH, Tq, Tk, d, causal, scale, s);
+}
+
+int fa_fwd_f32(const float *q, const float *k, const float *v, float *o, float *lse, int B, int H, int Tq, int Tk,
+               int d, int causal, float scale, fa_stream_t stream)
+{
+    int st = fa::check_fwd(q, k, v, o, lse, B, H, Tq, Tk, d, causal, scale, 4);
+    if (st != fa::OK)
+        return st;
+    const int BH = B * H;
+    if ((size_t)BH * Tq == 0)
+        return FA_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (Tk == 0)
+        return fa::fill_empty_launch(o, lse, (size_t)BH * Tq, d, 4, s);
+    return fa::fwd_f32_launch(q, k, v, o, lse, BH, Tq, Tk, d, causal, scale, s);
+}
+
+size_t fa_bwd_workspace_bytes(int B, int H, int Tq, int Tk, int d)
+{
+    if (B < 0 || H < 0 || Tq < 0 || Tk < 0 || (d != 64 && d != 128 && d != 256))
+        return 0;
+    return fa::bwd_workspace_bytes(B * H, Tq, d);
+}
+
+int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dO, void *dq,
+           void *dk, void *dv, int B, int H, int Tq, int Tk, int d, int causal, float scale, void *workspace,
+           size_t workspace_bytes, fa_stream_t stream)
+{
+    int st = fa::check_sizes(B, H, Tq, Tk, d, causal, scale);
+    if (st != fa::OK)
+        return st;
+    if (d == 256)
+        return FA_ERR_UNSUPPORTED;
+    const size_t bh = (size_t)B * H;
+    if (bh == 0 || (Tq == 0 && Tk == 0))
+        return FA_OK;
+    const size_t nq = bh * Tq * d * 2, nk = bh * Tk * d * 2, nl = bh * Tq * sizeof(float);
+    const size_t need = fa::bwd_workspace_bytes((int)bh, Tq, d);
+    if ((Tq > 0 && (!q || !o || !lse || !dO || !dq)) || (Tk > 0 && (!k || !v || !dk || !dv)) ||
+        (need > 0 && (!workspace || workspace_bytes < need)))
+        return FA_ERR_INVALID_ARG;
+    if (!fa::aligned16(q) || !fa::aligned16(k) || !fa::aligned16(v) || !fa::aligned16(o) || !fa::aligned16(lse) ||
+        !fa::aligned16(dO) || !fa::aligned16(dq) || !fa::aligned16(dk) || !fa::aligned16(dv) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return FA_ERR_INVALID_ARG;
+    const void *ins[6] = {q, k, v, o, lse, dO};
+    const size_t in_n[6] = {nq, nk, nk, nq, nl, nq};
+    void *outs[4] = {dq, dk, dv, workspace};
+    const size_t out_n[4] = {nq, nk, nk, need};
+    for (int i = 0; i < 4; ++i) {
+        for (int j = 0; j < 6; ++j)
+            if (fa::overlaps(outs[i], out_n[i], ins[j], in_n[j]))
+                return FA_ERR_INVALID_ARG;
+        for (int j = i + 1; j < 4; ++j)
+            if (fa::overlaps(outs[i], out_n[i], outs[j], out_n[j]))
+                return FA_ERR_INVALID_ARG;
+    }
+    st = fa::check_device();
+    if (st != fa::OK)
+        return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const fa::BwdWorkspace ws = fa::bwd_workspace_carve(workspace, (int)bh, Tq, d);
+    return fa::bwd_launch(q, k, v, o, lse, dO, dq, dk, dv, (int)bh, Tq, Tk, d, causal, scale, ws, s);
+}
+
+int fa_sync_status(fa_stream_t stream)
+{
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess)
+        return FA_ERR_CUDA;
+    int wf = 0, wb = 0;
+    if (fa::fwd_status_fetch_clear(s, &wf) != fa::OK || fa::bwd_status_fetch_clear(s, &wb) != fa::OK)
+        return FA_ERR_CUDA;
+    const int w = wf ? wf : wb;
+    return w ? (w & 0xFF) : FA_OK;
+}
+
+const char *fa_status_string(int status)
+{
+    switch (status) {
+    case FA_OK:
+        return "ok";
+    case FA_ERR_INVALID_ARG:
+        return "invalid argument (null or misaligned pointer, bad size or flag, overlapping output, bad scale)";
+    case FA_ERR_UNSUPPORTED:
+        return "unsupported (head width, backward d=256, or a device other than sm_103)";
+    case FA_ERR_CUDA:
+        return "CUDA runtime or driver error";
+    case FA_ERR_TIMEOUT:
+        return "a device-side bounded wait timed out; outputs of that call are invalid";
+    default:
+        return "unknown status";
+    }
+}
+
+}  // extern "C"

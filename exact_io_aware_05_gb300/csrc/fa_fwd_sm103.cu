@@ -1,0 +1,619 @@
+// fa_fwd_sm103.cu -- forward pass of IO-aware exact attention on sm_103a.
+//
+// What it computes (zerotofrontier.app "FlashAttention", Efficient attention
+// 12.3, section "The forward pass"): for every query block Q_i of 128 rows,
+// stream the key/value blocks K_j, V_j through shared memory and keep per
+// row a running maximum m, a running sum l and an unnormalised output O~:
+//     S_ij = Q_i K_j^T                    (tcgen05.mma, fp32 in tensor memory)
+//     m_new = max(m, rowmax(S_ij))
+//     P~ = exp(c S_ij - c m_new)          (exp2 with c*log2(e) folded in)
+//     l <- e^{c(m - m_new)} l + rowsum(P~),  O~ <- e^{c(m - m_new)} O~ + P~ V_j
+// then write O_i = O~ / l and lse_i = c m + log l once.  Causal tiles wholly
+// above the diagonal are never loaded or computed; the skip test compares the
+// first key of the block with the last query of the block ("The causal mask,
+// and the tiles you never visit").  The N x N matrices S and P never reach
+// HBM: S lives in tensor memory, P is written back over S as bf16 and fed to
+// the second MMA straight from tensor memory.
+//
+// GB300 design (differs from the pages' A100/H100 kernels):
+//   * persistent CTAs, one per SM, each owning a 256-row unit (two 128-row
+//     query tiles, d = 64/128) or a 128-row unit (d = 256); units are taken
+//     longest-first within groups of heads sized so their K/V stay in L2;
+//   * warp 0: TMA producer (Q once per unit, K/V tiles through an NSLOT-deep
+//     ring with full/empty mbarriers);
+//   * warp 1: a single thread issues every tcgen05.mma and commit;
+//   * one 128-thread softmax warpgroup per query tile (thread = query row =
+//     tensor-memory lane) doing the online softmax and the epilogue;
+//   * the rescale of O~ in tensor memory is skipped for a warp when none of
+//     its 32 rows saw its maximum grow (alpha = 1 exactly), so P~ <= 1 always
+//     and the largest weight of a row is exactly 1.0 in bf16.
+//   * every wait is bounded (see fa_common.cuh); on a timeout the CTA drains
+//     its in-flight copies and MMAs, frees tensor memory and returns.
+#include "fa_common.cuh"
+#include "fa_internal.h"
+
+namespace fa {
+
+__device__ int g_fwd_status;   // device status word of the forward kernels
+
+namespace {
+
+constexpr int BR = 128;                 // query rows per tile (= MMA M = TMEM lanes)
+
+template <int D>
+struct FwdCfg;
+template <>
+struct FwdCfg<64> {
+    static constexpr int BC = 128, NQ = 2, NSLOT = 8;
+};
+template <>
+struct FwdCfg<128> {
+    static constexpr int BC = 128, NQ = 2, NSLOT = 4;
+};
+template <>
+struct FwdCfg<256> {
+    static constexpr int BC = 64, NQ = 1, NSLOT = 4;
+};
+
+template <int D>
+struct FwdLayout {
+    using C = FwdCfg<D>;
+    static constexpr int BC = C::BC, NQ = C::NQ, NSLOT = C::NSLOT;
+    static constexpr int KCH = D / 64;                 // 64-column (128-byte) chunks per row
+    static constexpr int Q_CHUNK = BR * 128;
+    static constexpr int Q_TILE = KCH * Q_CHUNK;
+    static constexpr int KV_CHUNK = BC * 128;
+    static constexpr int KV_TILE = KCH * KV_CHUNK;
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_SLOT = NQ * Q_TILE;
+    static constexpr int OFF_BAR = OFF_SLOT + NSLOT * KV_TILE;
+    // barrier indices
+    static constexpr int B_FULL = 0, B_EMPTY = NSLOT, B_QFULL = 2 * NSLOT, B_QEMPTY = 2 * NSLOT + 1,
+                         B_SFULL = 2 * NSLOT + 2, B_PFULL = 2 * NSLOT + 4, B_ODONE = 2 * NSLOT + 6,
+                         B_OEMPTY = 2 * NSLOT + 8, B_DRAIN = 2 * NSLOT + 10, B_PREAD = 2 * NSLOT + 11,
+                         B_OFINAL = 2 * NSLOT + 13, NBAR = 2 * NSLOT + 15;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;   // tmem base (u32), abort flag (int)
+    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1024-byte alignment
+    static constexpr int S_COL = 0;                  // S buffer b at columns [b*BC, (b+1)*BC)
+    static constexpr int O_COL = 2 * BC;             // O~ of tile t at [O_COL + t*D, +D)
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int NTHREADS = 128 + NQ * 128;
+    static_assert(O_COL + NQ * D <= TMEM_COLS, "tensor memory budget");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+    static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BC, false, false);   // Q K^T, both K-major
+    static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, false, true);    // P V, V is MN-major
+};
+
+enum WaitSite : int {
+    SITE_P_EMPTY = 1, SITE_P_QEMPTY, SITE_M_QFULL, SITE_M_FULL, SITE_M_PFULL, SITE_M_OEMPTY,
+    SITE_S_SFULL, SITE_S_ODONE, SITE_S_EPI, SITE_M_PREAD
+};
+
+struct FwdArgs {
+    __nv_bfloat16 *o;
+    float *lse;
+    int BH, Tq, Tk, causal;
+    float scale_log2;    // scale * log2(e)
+    int nqb;             // units per head
+    int units;           // BH * nqb
+    int group;           // heads per L2 group
+    uint64_t timeout_ns;
+};
+
+// One unit = NQ consecutive 128-row query tiles of one (b, h).
+struct Plan {
+    int bh, row0;
+    int n[2];       // KV tiles needed by tile t (0: none)
+    int rows[2];    // tile t has at least one query row
+    int J;          // jobs (one S and one PV MMA each) in the unit
+};
+
+template <int D>
+__device__ __forceinline__ Plan make_plan(int u, const FwdArgs &a)
+{
+    using L = FwdLayout<D>;
+    const int per_group = a.group * a.nqb;
+    const int g = u / per_group;
+    const int w = u - g * per_group;
+    const int heads_here = min(a.group, a.BH - g * a.group);
+    const int lvl = w / heads_here;                // 0 = longest units first
+    Plan p;
+    p.bh = g * a.group + (w - lvl * heads_here);
+    const int qb = a.nqb - 1 - lvl;
+    p.row0 = qb * L::NQ * BR;
+    const int nkv = (a.Tk + L::BC - 1) / L::BC;
+    p.J = 0;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const int r_first = p.row0 + t * BR;
+        p.rows[t] = (t < L::NQ) && (r_first < a.Tq);
+        int n = 0;
+        if (p.rows[t]) {
+            if (!a.causal) {
+                n = nkv;
+            } else {
+                const int r_last = min(r_first + BR - 1, a.Tq - 1);
+                const long lim = (long)r_last + a.Tk - a.Tq;   // last allowed key of the last row
+                n = lim < 0 ? 0 : min(nkv, (int)(lim / L::BC) + 1);
+            }
+        }
+        p.n[t] = n;
+        p.J += n;
+    }
+    return p;
+}
+
+// Job k of a unit -> (query tile t, key block j); first/last: whether this job
+// is the first/last user of K_j (S MMA order) and of V_j (PV MMA order).
+template <int NQ>
+__device__ __forceinline__ void job_of(const Plan &p, int k, int &t, int &j, bool &first, bool &last)
+{
+    if constexpr (NQ == 1) {
+        t = 0;
+        j = k;
+        first = last = true;
+    } else {
+        const int a = min(p.n[0], p.n[1]);
+        if (k < 2 * a) {
+            t = k & 1;
+            j = k >> 1;
+            first = (t == 0);
+            last = (t == 1);
+        } else {
+            t = (p.n[0] > p.n[1]) ? 0 : 1;
+            j = a + (k - 2 * a);
+            first = last = true;
+        }
+    }
+}
+
+// The MMA order of a unit: S(0), S(1), then PV(k) followed by S(k+2).  The
+// producer walks the same order to load tiles in first-use order.
+template <typename FS, typename FPV>
+__device__ __forceinline__ bool walk_ops(int J, FS &&fs, FPV &&fpv)
+{
+    if (!fs(0))
+        return false;
+    if (J > 1 && !fs(1))
+        return false;
+    for (int k = 0; k < J; ++k) {
+        if (!fpv(k))
+            return false;
+        if (k + 2 < J && !fs(k + 2))
+            return false;
+    }
+    return true;
+}
+
+template <int D>
+__global__ void __launch_bounds__(FwdLayout<D>::NTHREADS, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const FwdArgs a)
+{
+    using L = FwdLayout<D>;
+    constexpr int BC = L::BC, NQ = L::NQ, NSLOT = L::NSLOT;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (sbase - raw);
+    const uint32_t bar0 = sbase + L::OFF_BAR;
+    auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
+
+    const uint32_t warp = warp_id(), lane = lane_id();
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NSLOT; ++s) {
+            mbar_init(bar(L::B_FULL + s), 1);
+            mbar_init(bar(L::B_EMPTY + s), 1);
+        }
+        mbar_init(bar(L::B_QFULL), 1);
+        mbar_init(bar(L::B_QEMPTY), 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(L::B_SFULL + b), 1);
+            mbar_init(bar(L::B_PFULL + b), 128);
+            mbar_init(bar(L::B_ODONE + b), 1);
+            mbar_init(bar(L::B_OEMPTY + b), 128);
+        }
+        mbar_init(bar(L::B_PREAD), 1);
+        mbar_init(bar(L::B_PREAD + 1), 1);
+        mbar_init(bar(L::B_OFINAL), 1);
+        mbar_init(bar(L::B_OFINAL + 1), 1);
+        mbar_init(bar(L::B_DRAIN), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), L::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtx ctx{abort_flag, &g_fwd_status, a.timeout_ns};
+
+    uint32_t n_loads = 0, n_q = 0;   // producer counters, kept for the drain
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t pol_kv = policy_evict_last();
+            const uint64_t pol_q = policy_evict_first();
+            for (int u = blockIdx.x; u < a.units; u += gridDim.x) {
+                const Plan p = make_plan<D>(u, a);
+                if (p.J == 0)
+                    continue;
+                if (n_q > 0 && !mbar_wait(bar(L::B_QEMPTY), (n_q - 1) & 1, ctx, SITE_P_QEMPTY))
+                    break;
+                uint32_t qbytes = 0;
+                for (int t = 0; t < NQ; ++t)
+                    qbytes += p.n[t] > 0 ? L::Q_TILE : 0;
+                mbar_arrive_expect_tx(bar(L::B_QFULL), qbytes);
+                for (int t = 0; t < NQ; ++t)
+                    if (p.n[t] > 0)
+                        for (int c = 0; c < L::KCH; ++c)
+                            tma_load_3d_hint(sbase + L::OFF_Q + t * L::Q_TILE + c * L::Q_CHUNK, &tm_q,
+                                             bar(L::B_QFULL), c * 64, p.row0 + t * BR, p.bh, pol_q);
+                ++n_q;
+                auto load = [&](const CUtensorMap *map, int j) -> bool {
+                    const uint32_t slot = n_loads % NSLOT;
+                    if (n_loads >= NSLOT &&
+                        !mbar_wait(bar(L::B_EMPTY + slot), ((n_loads / NSLOT) - 1) & 1, ctx, SITE_P_EMPTY))
+                        return false;
+                    mbar_arrive_expect_tx(bar(L::B_FULL + slot), L::KV_TILE);
+                    const uint32_t dst = sbase + L::OFF_SLOT + slot * L::KV_TILE;
+                    for (int c = 0; c < L::KCH; ++c)
+                        tma_load_3d_hint(dst + c * L::KV_CHUNK, map, bar(L::B_FULL + slot), c * 64,
+                                         j * BC, p.bh, pol_kv);
+                    ++n_loads;
+                    return true;
+                };
+                const bool ok = walk_ops(
+                    p.J,
+                    [&](int k) {
+                        int t, j;
+                        bool first, last;
+                        job_of<NQ>(p, k, t, j, first, last);
+                        return first ? load(&tm_k, j) : true;
+                    },
+                    [&](int k) {
+                        int t, j;
+                        bool first, last;
+                        job_of<NQ>(p, k, t, j, first, last);
+                        return first ? load(&tm_v, j) : true;
+                    });
+                if (!ok)
+                    break;
+            }
+            // drain: every copy still in flight lands before the CTA exits
+            const uint32_t lo = n_loads > (uint32_t)NSLOT ? n_loads - NSLOT : 0;
+            for (uint32_t i = lo; i < n_loads; ++i)
+                mbar_wait_drain(bar(L::B_FULL + i % NSLOT), (i / NSLOT) & 1, a.timeout_ns);
+            if (n_q > 0)
+                mbar_wait_drain(bar(L::B_QFULL), (n_q - 1) & 1, a.timeout_ns);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t ld = 0, kg = 0, q_seen = 0;
+            uint32_t epi[2] = {0, 0};
+            for (int u = blockIdx.x; u < a.units; u += gridDim.x) {
+                const Plan p = make_plan<D>(u, a);
+                if (p.J == 0)
+                    continue;
+                if (!mbar_wait(bar(L::B_QFULL), q_seen & 1, ctx, SITE_M_QFULL))
+                    break;
+                ++q_seen;
+                uint32_t kslot = 0, vslot = 0;
+                auto acquire = [&](uint32_t &slot) -> bool {
+                    slot = ld % NSLOT;
+                    const bool ok = mbar_wait(bar(L::B_FULL + slot), (ld / NSLOT) & 1, ctx, SITE_M_FULL);
+                    ++ld;
+                    return ok;
+                };
+                const bool ok = walk_ops(
+                    p.J,
+                    [&](int k) -> bool {
+                        int t, j;
+                        bool first, last;
+                        job_of<NQ>(p, k, t, j, first, last);
+                        if (first && !acquire(kslot))
+                            return false;
+                        const uint32_t b = (kg + k) & 1;
+                        // S overwrites the columns that held P of job (kg + k - 2): that PV
+                        // must have finished reading them
+                        const uint32_t g = kg + k;
+                        if (g >= 2 && !mbar_wait(bar(L::B_PREAD + b), ((g - 2) >> 1) & 1, ctx, SITE_M_PREAD))
+                            return false;
+                        tc_fence_after();
+                        const uint32_t qa = sbase + L::OFF_Q + t * L::Q_TILE;
+                        const uint32_t ka = sbase + L::OFF_SLOT + kslot * L::KV_TILE;
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = (kk & 3) * 32;   // 16 bf16 = 32 bytes along K
+                            const uint64_t ad = sdesc_sw128(qa + (kk >> 2) * L::Q_CHUNK + off, 16, 1024);
+                            const uint64_t bd = sdesc_sw128(ka + (kk >> 2) * L::KV_CHUNK + off, 16, 1024);
+                            mma_ss(tmem + L::S_COL + b * BC, ad, bd, L::IDESC_S, kk > 0 ? 1u : 0u);
+                        }
+                        tc_commit(bar(L::B_SFULL + b));
+                        if (last)
+                            tc_commit(bar(L::B_EMPTY + kslot));
+                        if (k == p.J - 1)
+                            tc_commit(bar(L::B_QEMPTY));
+                        return true;
+                    },
+                    [&](int k) -> bool {
+                        int t, j;
+                        bool first, last;
+                        job_of<NQ>(p, k, t, j, first, last);
+                        if (first && !acquire(vslot))
+                            return false;
+                        const uint32_t b = (kg + k) & 1;
+                        if (!mbar_wait(bar(L::B_PFULL + b), ((kg + k) >> 1) & 1, ctx, SITE_M_PFULL))
+                            return false;
+                        if (j == 0 && epi[t] > 0 &&
+                            !mbar_wait(bar(L::B_OEMPTY + t), (epi[t] - 1) & 1, ctx, SITE_M_OEMPTY))
+                            return false;
+                        tc_fence_after();
+                        const uint32_t va = sbase + L::OFF_SLOT + vslot * L::KV_TILE;
+#pragma unroll
+                        for (int kk = 0; kk < BC / 16; ++kk) {
+                            const uint64_t bd = sdesc_sw128(va + kk * 16 * 128, L::KV_CHUNK, 1024);
+                            mma_ts(tmem + L::O_COL + t * D, tmem + L::S_COL + b * BC + kk * 8, bd,
+                                   L::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        tc_commit(bar(L::B_ODONE + t));
+                        tc_commit(bar(L::B_PREAD + b));
+                        if (last)
+                            tc_commit(bar(L::B_EMPTY + vslot));
+                        if (j == p.n[t] - 1) {   // last PV of this tile in the unit
+                            tc_commit(bar(L::B_OFINAL + t));
+                            ++epi[t];
+                        }
+                        return true;
+                    });
+                if (!ok)
+                    break;
+                kg += p.J;
+            }
+            // drain: all issued MMAs complete before tensor memory is released
+            tc_commit(bar(L::B_DRAIN));
+            mbar_wait_drain(bar(L::B_DRAIN), 0, a.timeout_ns);
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ------------------------------------------------ softmax + epilogue
+        const int t = (int)(warp - 4) >> 2;            // query tile of this warpgroup
+        const uint32_t quarter = warp & 3u;            // TMEM lanes [32*quarter, +32)
+        const int rit = (int)(quarter * 32 + lane);    // row within the tile
+        const float sl2 = a.scale_log2;
+        const uint32_t lane_base = tmem + ((quarter * 32u) << 16);
+        uint32_t kg = 0, pv = 0, ep = 0;
+        for (int u = blockIdx.x; u < a.units; u += gridDim.x) {
+            const Plan p = make_plan<D>(u, a);
+            const int r = p.row0 + t * BR + rit;
+            const bool row_ok = r < a.Tq;
+            const size_t grow = (size_t)p.bh * a.Tq + r;
+            if (!p.rows[t]) {
+                kg += p.J;
+                continue;
+            }
+            if (p.n[t] == 0) {   // no key is allowed for any row of this tile
+                if (row_ok) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(a.o + grow * D);
+                    for (int i = 0; i < D / 8; ++i)
+                        dst[i] = make_uint4(0, 0, 0, 0);
+                    a.lse[grow] = -INFINITY;
+                }
+                kg += p.J;
+                continue;
+            }
+            float m = -INFINITY, l = 0.f;
+            bool ok = true;
+            for (int k = 0; k < p.J && ok; ++k) {
+                int tt, j;
+                bool first, last;
+                job_of<NQ>(p, k, tt, j, first, last);
+                if (tt != t)
+                    continue;
+                const uint32_t b = (kg + k) & 1;
+                if (!mbar_wait(bar(L::B_SFULL + b), ((kg + k) >> 1) & 1, ctx, SITE_S_SFULL)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                float s[BC];
+#pragma unroll
+                for (int c = 0; c < BC / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld_x32(lane_base + L::S_COL + b * BC + c * 32, v);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        s[c * 32 + i] = __uint_as_float(v[i]);
+                }
+                // mask: tail keys beyond Tk, and keys after the causal limit
+                const int kv0 = j * BC;
+                const int first_row = p.row0 + t * BR;
+                const bool need_mask = (kv0 + BC > a.Tk) ||
+                                       (a.causal && (long)kv0 + BC - 1 > (long)first_row + a.Tk - a.Tq);
+                if (need_mask) {
+                    long lim = a.Tk;
+                    if (a.causal)
+                        lim = min(lim, (long)r + a.Tk - a.Tq + 1);
+                    const int cl = (int)max(0L, min((long)BC, lim - kv0));   // columns < cl are allowed
+#pragma unroll
+                    for (int i = 0; i < BC; ++i)
+                        if (i >= cl)
+                            s[i] = -INFINITY;
+                }
+                float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+                for (int i = 4; i < BC; i += 4) {
+                    mx0 = fmaxf(mx0, s[i]);
+                    mx1 = fmaxf(mx1, s[i + 1]);
+                    mx2 = fmaxf(mx2, s[i + 2]);
+                    mx3 = fmaxf(mx3, s[i + 3]);
+                }
+                const float m_new = fmaxf(m, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)));
+                const bool resc = (m != -INFINITY) && (m_new > m);
+                float alpha = 1.f;
+                if (m == -INFINITY) {
+                    m = m_new;                     // O~ and l of this row are still exactly 0
+                } else if (resc) {
+                    alpha = ex2_approx((m - m_new) * sl2);
+                    l *= alpha;
+                    m = m_new;
+                }
+                // P~ = exp2(c log2e (s - m)), packed to bf16 pairs over the first BC/2
+                // columns of this S buffer, 32 keys at a time
+                const float mref = (m == -INFINITY) ? 0.f : m * sl2;
+                float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+                for (int c = 0; c < BC / 32; ++c) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float p0 = ex2_approx(fmaf(s[c * 32 + 2 * i], sl2, -mref));
+                        const float p1 = ex2_approx(fmaf(s[c * 32 + 2 * i + 1], sl2, -mref));
+                        l0 += p0;
+                        l1 += p1;
+                        pk[i] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st_x16(lane_base + L::S_COL + b * BC + c * 16, pk);
+                }
+                l += l0 + l1;
+                if (__any_sync(0xffffffffu, resc)) {
+                    // O~ must hold the previous PV of this tile before it is rescaled
+                    if (!mbar_wait(bar(L::B_ODONE + t), (pv - 1) & 1, ctx, SITE_S_ODONE)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t v[32];
+                        const uint32_t ta = lane_base + L::O_COL + t * D + c * 32;
+                        tmem_ld_x32(ta, v);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+                        tmem_st_x32(ta, v);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(bar(L::B_PFULL + b));
+                ++pv;
+            }
+            if (!ok)
+                break;
+            // epilogue: O = O~ / l, lse = c m + ln l.  The softmax can be up to two PVs
+            // ahead of the tensor core here, too far for a parity wait on the per-PV
+            // barrier; the per-unit barrier completes exactly once per epilogue.
+            if (!mbar_wait(bar(L::B_OFINAL + t), ep & 1, ctx, SITE_S_EPI))
+                break;
+            ++ep;
+            tc_fence_after();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld_x32(lane_base + L::O_COL + t * D + c * 32, v);
+                if (row_ok) {
+                    uint32_t w[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        w[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * inv, __uint_as_float(v[2 * i + 1]) * inv);
+                    uint4 *dst = reinterpret_cast<uint4 *>(a.o + grow * D + c * 32);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                }
+            }
+            if (row_ok)
+                a.lse[grow] = l > 0.f ? (m * sl2 + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+            tc_fence_before();
+            mbar_arrive(bar(L::B_OEMPTY + t));
+            kg += p.J;
+        }
+    }
+    // ---------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, L::TMEM_COLS);
+    }
+}
+
+template <int D>
+int launch(const void *q, const void *k, const void *v, void *o, float *lse, int BH, int Tq, int Tk,
+           int causal, float scale, cudaStream_t s)
+{
+    using L = FwdLayout<D>;
+    CUtensorMap tq, tk, tv;
+    int st = encode_tmap_3d(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, Tq, BH, 64, BR);
+    if (st == OK)
+        st = encode_tmap_3d(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, Tk, BH, 64, L::BC);
+    if (st == OK)
+        st = encode_tmap_3d(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, Tk, BH, 64, L::BC);
+    if (st != OK)
+        return st;
+    FwdArgs a;
+    a.o = static_cast<__nv_bfloat16 *>(o);
+    a.lse = lse;
+    a.BH = BH;
+    a.Tq = Tq;
+    a.Tk = Tk;
+    a.causal = causal;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.nqb = (Tq + L::NQ * BR - 1) / (L::NQ * BR);
+    a.units = BH * a.nqb;
+    // heads per group: keep the group's K and V within ~48 MB of L2
+    const double kv_head = 2.0 * Tk * D * 2.0;
+    int g = (int)(48.0 * 1024 * 1024 / (kv_head > 1 ? kv_head : 1));
+    a.group = g < 1 ? 1 : (g > BH ? BH : g);
+    a.timeout_ns = wait_timeout_ns();
+    const int grid = a.units < device_sm_count() ? a.units : device_sm_count();
+    if (cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             L::SMEM_BYTES) != cudaSuccess)
+        return ERR_CUDA;
+    fwd_kernel<D><<<grid, L::NTHREADS, L::SMEM_BYTES, s>>>(tq, tk, tv, a);
+    return cudaGetLastError() == cudaSuccess ? OK : ERR_CUDA;
+}
+
+}  // namespace
+
+int fwd_bf16_launch(const void *q, const void *k, const void *v, void *o, float *lse, int BH, int Tq,
+                    int Tk, int d, int causal, float scale, cudaStream_t s)
+{
+    switch (d) {
+    case 64:
+        return launch<64>(q, k, v, o, lse, BH, Tq, Tk, causal, scale, s);
+    case 128:
+        return launch<128>(q, k, v, o, lse, BH, Tq, Tk, causal, scale, s);
+    case 256:
+        return launch<256>(q, k, v, o, lse, BH, Tq, Tk, causal, scale, s);
+    default:
+        return ERR_UNSUPPORTED;
+    }
+}
+
+int fwd_status_fetch_clear(cudaStream_t s, int *host_word)
+{
+    int zero = 0;
+    if (cudaMemcpyFromSymbolAsync(host_word, g_fwd_status, sizeof(int), 0, cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess ||
+        cudaMemcpyToSymbolAsync(g_fwd_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return ERR_CUDA;
+    return OK;
+}
+
+}  // namespace fa

@@ -1,0 +1,50 @@
+// fa_internal.h -- host-side glue between the C-ABI layer (fa_api.cu) and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace fa {
+
+// Status codes, identical to fa_status in include/fa.h.
+enum : int { OK = 0, ERR_INVALID_ARG = 1, ERR_UNSUPPORTED = 2, ERR_CUDA = 3, ERR_TIMEOUT = 4 };
+
+// Encodes a 3-D tiled TMA map over a contiguous [planes][rows][inner] tensor
+// with 128-byte swizzle; the box is [1][box_rows][box_inner].  Returns OK or
+// ERR_CUDA (driver entry point missing, or the driver rejected the map).
+int encode_tmap_3d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes,
+                   uint64_t inner, uint64_t rows, uint64_t planes, uint32_t box_inner,
+                   uint32_t box_rows);
+
+int device_sm_count();          // SMs of the current device (cached per device)
+uint64_t wait_timeout_ns();     // bounded-wait limit for device spin waits
+
+// Kernel launchers (arguments already validated by the ABI layer).
+int fwd_bf16_launch(const void *q, const void *k, const void *v, void *o, float *lse, int BH,
+                    int Tq, int Tk, int d, int causal, float scale, cudaStream_t s);
+int fwd_f32_launch(const float *q, const float *k, const float *v, float *o, float *lse, int BH,
+                   int Tq, int Tk, int d, int causal, float scale, cudaStream_t s);
+int fill_empty_launch(void *o, float *lse, size_t rows, int d, int elem_bytes, cudaStream_t s);
+
+// Backward workspace; rows of every head are padded to Tq_pad = roundup(Tq, 128).
+struct BwdWorkspace {
+    float *lse2;     // [BH][Tq_pad]    lse * log2(e); +inf for padding rows and rows without keys
+    float *delta;    // [BH][Tq_pad]    D_r = dO_r . O_r (0 for padding rows)
+    float *dq_acc;   // [BH][Tq_pad][d] fp32 dQ accumulator (unscaled)
+};
+size_t bwd_row_stride(int Tq);
+size_t bwd_workspace_bytes(int BH, int Tq, int d);
+BwdWorkspace bwd_workspace_carve(void *ws, int BH, int Tq, int d);
+int bwd_launch(const void *q, const void *k, const void *v, const void *o, const float *lse,
+               const void *dO, void *dq, void *dk, void *dv, int BH, int Tq, int Tk, int d,
+               int causal, float scale, const BwdWorkspace &ws, cudaStream_t s);
+
+// Device status words of the kernel translation units: read, add into *acc
+// the first nonzero value, and clear.  Stream-ordered; the caller syncs.
+int fwd_status_fetch_clear(cudaStream_t s, int *host_word);
+int bwd_status_fetch_clear(cudaStream_t s, int *host_word);
+
+}  // namespace fa

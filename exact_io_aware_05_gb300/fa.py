@@ -1,0 +1,162 @@
+"""ctypes binding of libfa.so (include/fa.h): argument marshalling only.
+
+Every function here checks tensor dtypes, shapes, devices and contiguity,
+reads the current CUDA stream, and calls the C entry point of the same name
+with raw device pointers.  No attention arithmetic happens in Python and
+there is no fallback: importing this module fails if libfa.so is missing,
+and every nonzero status raises ``FAError``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfa.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is not built; run exact_io_aware_05_gb300.build.build() "
+                      "(or __graft_entry__.build()) first")
+
+_lib = ctypes.CDLL(LIB_PATH)
+_vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+_lib.fa_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp]
+_lib.fa_fwd.restype = _i
+_lib.fa_fwd_f32.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp]
+_lib.fa_fwd_f32.restype = _i
+_lib.fa_bwd_workspace_bytes.argtypes = [_i, _i, _i, _i, _i]
+_lib.fa_bwd_workspace_bytes.restype = _sz
+_lib.fa_bwd.argtypes = [_vp] * 9 + [_i] * 6 + [_f, _vp, _sz, _vp]
+_lib.fa_bwd.restype = _i
+_lib.fa_sync_status.argtypes = [_vp]
+_lib.fa_sync_status.restype = _i
+_lib.fa_status_string.argtypes = [_i]
+_lib.fa_status_string.restype = ctypes.c_char_p
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
+
+
+class FAError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {_lib.fa_status_string(status).decode()} (status {status})")
+
+
+def lib() -> ctypes.CDLL:
+    return _lib
+
+
+def _check(fn: str, st: int) -> None:
+    if st != FA_OK:
+        raise FAError(fn, st)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype, shape: tuple, device: torch.device) -> None:
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.device != device:
+        raise ValueError(f"{name}: expected device {device}, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+
+
+def _shapes(q, k):
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q, k must be [B, H, T, d]")
+    B, H, Tq, d = q.shape
+    Tk = k.shape[2]
+    return B, H, Tq, Tk, d
+
+
+def fa_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
+    """O and lse for bf16 q [B,H,Tq,d], k/v [B,H,Tk,d]; o bf16 like q, lse f32 [B,H,Tq]."""
+    B, H, Tq, Tk, d = _shapes(q, k)
+    dev = q.device
+    _need(q, "q", torch.bfloat16, (B, H, Tq, d), dev)
+    _need(k, "k", torch.bfloat16, (B, H, Tk, d), dev)
+    _need(v, "v", torch.bfloat16, (B, H, Tk, d), dev)
+    _need(o, "o", torch.bfloat16, (B, H, Tq, d), dev)
+    _need(lse, "lse", torch.float32, (B, H, Tq), dev)
+    _check("fa_fwd", _lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Tq, Tk, d,
+                                 int(bool(causal)), float(scale), _stream(stream)))
+
+
+def fa_fwd_f32(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
+    """fp32 SIMT forward (precision reference path); all tensors float32."""
+    B, H, Tq, Tk, d = _shapes(q, k)
+    dev = q.device
+    _need(q, "q", torch.float32, (B, H, Tq, d), dev)
+    _need(k, "k", torch.float32, (B, H, Tk, d), dev)
+    _need(v, "v", torch.float32, (B, H, Tk, d), dev)
+    _need(o, "o", torch.float32, (B, H, Tq, d), dev)
+    _need(lse, "lse", torch.float32, (B, H, Tq), dev)
+    _check("fa_fwd_f32", _lib.fa_fwd_f32(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Tq, Tk,
+                                         d, int(bool(causal)), float(scale), _stream(stream)))
+
+
+def fa_bwd_workspace_bytes(B: int, H: int, Tq: int, Tk: int, d: int) -> int:
+    return int(_lib.fa_bwd_workspace_bytes(B, H, Tq, Tk, d))
+
+
+def fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, causal: bool, scale: float, workspace: torch.Tensor,
+           stream=None) -> None:
+    """dQ, dK, dV (bf16) from bf16 q, k, v, o, dO and the f32 lse of fa_fwd."""
+    B, H, Tq, Tk, d = _shapes(q, k)
+    dev = q.device
+    for name, t, shp in (("q", q, (B, H, Tq, d)), ("k", k, (B, H, Tk, d)), ("v", v, (B, H, Tk, d)),
+                         ("o", o, (B, H, Tq, d)), ("dO", dO, (B, H, Tq, d)), ("dq", dq, (B, H, Tq, d)),
+                         ("dk", dk, (B, H, Tk, d)), ("dv", dv, (B, H, Tk, d))):
+        _need(t, name, torch.bfloat16, shp, dev)
+    _need(lse, "lse", torch.float32, (B, H, Tq), dev)
+    if workspace.device != dev or not workspace.is_contiguous():
+        raise ValueError("workspace: must be a contiguous tensor on the same device")
+    nbytes = workspace.numel() * workspace.element_size()
+    _check("fa_bwd", _lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
+                                 _ptr(dk), _ptr(dv), B, H, Tq, Tk, d, int(bool(causal)), float(scale),
+                                 _ptr(workspace), nbytes, _stream(stream)))
+
+
+def fa_sync_status(stream=None) -> int:
+    return int(_lib.fa_sync_status(_stream(stream)))
+
+
+def fa_status_string(status: int) -> str:
+    return _lib.fa_status_string(status).decode()
+
+
+# ---------------------------------------------------------------- conveniences
+def attention_forward(q, k, v, causal: bool, scale: float, stream=None):
+    """Allocates O and lse with torch and runs fa_fwd (bf16) or fa_fwd_f32 (float32)."""
+    B, H, Tq, Tk, d = _shapes(q, k)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Tq), dtype=torch.float32, device=q.device)
+    (fa_fwd_f32 if q.dtype == torch.float32 else fa_fwd)(q, k, v, o, lse, causal, scale, stream)
+    return o, lse
+
+
+def alloc_workspace(B, H, Tq, Tk, d, device) -> torch.Tensor:
+    n = fa_bwd_workspace_bytes(B, H, Tq, Tk, d)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def attention_backward(q, k, v, o, lse, dO, causal: bool, scale: float, workspace=None, stream=None):
+    """Allocates dQ, dK, dV (and the workspace if not given) and runs fa_bwd."""
+    B, H, Tq, Tk, d = _shapes(q, k)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = alloc_workspace(B, H, Tq, Tk, d, q.device) if workspace is None else workspace
+    fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, causal, scale, ws, stream)
+    return dq, dk, dv

@@ -1,0 +1,114 @@
+/*
+ * fa.h -- C ABI of libfa.so: IO-aware exact attention for GB300 (sm_103a).
+ *
+ * Every tensor is a plain device pointer to a contiguous row-major array:
+ *   q, o, dO, dq : [B][H][Tq][d]      k, v, dk, dv : [B][H][Tk][d]
+ *   lse          : [B][H][Tq] float32 (natural-log log-sum-exp of the scaled scores)
+ * "bf16" tensors hold IEEE bfloat16 values; "f32" tensors hold float32.
+ * Every base pointer must be 16-byte aligned.
+ *
+ * Semantics.  S = scale * Q K^T per (b, h); P = softmax(S) row-wise over the
+ * allowed keys; O = P V; lse_r = log sum_l exp(S_rl).  With causal != 0 key l
+ * is allowed for query r iff l <= r + (Tk - Tq) (bottom-right alignment; for
+ * Tq == Tk this is "query r sees keys l <= r").  A query row with no allowed
+ * key gets O = 0, lse = -inf and zero gradients.  scale must be finite and
+ * > 0 (the usual value is 1/sqrt(d)); there is no implicit default.
+ *
+ * Sources (page titles and sections):
+ *   zerotofrontier.app "FlashAttention" (Efficient attention 12.3):
+ *     "The forward pass" -- O_i = diag(l)^-1 O~ and lse_i = m + log l written once;
+ *     "The causal mask, and the tiles you never visit" -- the three tile kinds;
+ *     "What the forward pass leaves behind" -- O plus one lse per row is all
+ *       the backward pass needs;
+ *     "The backward pass, derived" -- D_r = dO_r . O_r, dS = P o (dP - D),
+ *       key blocks outside, dQ accumulated by atomic additions.
+ *   atlas.blal.pro "FlashAttention -- IO-Aware Exact Attention":
+ *     "Online softmax" and "Recomputation in the backward pass".
+ *
+ * Ownership.  The caller allocates and owns every buffer, including the
+ * backward workspace.  The library keeps no per-call state; tensor maps are
+ * built on the host per call and passed by value.  Calls are thread-safe.
+ *
+ * Errors.  Calls are asynchronous on `stream` (a cudaStream_t; NULL is the
+ * legacy default stream).  The return value reports argument validation and
+ * launch errors only.  A device-side failure (a bounded wait that timed out)
+ * is recorded in a per-device status word and returned by fa_sync_status().
+ * On any nonzero return, no kernel was launched and outputs are untouched,
+ * except FA_ERR_CUDA from a failed launch.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size, aliasing outputs, bad scale */
+    FA_ERR_UNSUPPORTED = 2,   /* head width not supported, or the device is not sm_103 */
+    FA_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed */
+    FA_ERR_TIMEOUT = 4        /* a device-side bounded wait ran out (from fa_sync_status) */
+} fa_status;
+
+typedef struct CUstream_st *fa_stream_t;   /* identical to cudaStream_t */
+
+/*
+ * Forward pass, bf16 in / bf16 O / f32 lse, fp32 accumulation on tcgen05
+ * tensor cores.  d in {64, 128, 256}.  B, H, Tq, Tk >= 0; a call with
+ * B*H*Tq == 0 is a no-op; Tk == 0 writes O = 0 and lse = -inf.
+ * o and lse must not overlap q, k, v or each other.
+ */
+int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+           int B, int H, int Tq, int Tk, int d, int causal, float scale,
+           fa_stream_t stream);
+
+/*
+ * Forward pass with f32 tensors and plain fp32 FFMA arithmetic (no tensor
+ * cores): the debug/reference-precision build of the same tiled online
+ * softmax.  Same shapes, rules and errors as fa_fwd.
+ */
+int fa_fwd_f32(const float *q, const float *k, const float *v, float *o, float *lse,
+               int B, int H, int Tq, int Tk, int d, int causal, float scale,
+               fa_stream_t stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs for these sizes: a log2-domain copy
+ * of lse and the row terms D (each [B][H][Tq_pad] f32) and the fp32 dQ
+ * accumulator [B][H][Tq_pad][d], where Tq_pad rounds Tq up to a multiple of 128;
+ * each region is 256-byte aligned.  Returns 0 for
+ * invalid sizes.
+ */
+size_t fa_bwd_workspace_bytes(int B, int H, int Tq, int Tk, int d);
+
+/*
+ * Backward pass, bf16 q, k, v, o, dO, dq, dk, dv; f32 lse.  o and lse must be
+ * what fa_fwd returned for the same q, k, v, causal and scale.  d in {64, 128}
+ * (d = 256 returns FA_ERR_UNSUPPORTED).  workspace must hold at least
+ * fa_bwd_workspace_bytes(...) bytes, 256-byte aligned; its contents on entry
+ * are ignored.  dq, dk, dv must not overlap any input, the workspace or each
+ * other.  dQ is accumulated with fp32 atomic additions, so its last bits may
+ * differ from run to run.
+ */
+int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+           const void *dO, void *dq, void *dk, void *dv,
+           int B, int H, int Tq, int Tk, int d, int causal, float scale,
+           void *workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the device status word of
+ * the current device: FA_OK, FA_ERR_TIMEOUT (a kernel's bounded wait ran out;
+ * its outputs are invalid) or FA_ERR_CUDA (the synchronise failed).
+ */
+int fa_sync_status(fa_stream_t stream);
+
+/* Static, never-NULL description of a status code. */
+const char *fa_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

@@ -1,0 +1,92 @@
+"""The C ABI without a GPU: libfa.so builds, loads, exports every function that
+include/fa.h declares, and rejects bad arguments on the host before any CUDA
+call (so these run on a CPU-only machine)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_io_aware_05_gb300 import build
+    so = build.build()
+    return ctypes.CDLL(so)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(fa_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("fa_fwd", "fa_bwd", "fa_fwd_f32", "fa_bwd_workspace_bytes", "fa_sync_status", "fa_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+
+
+def _fwd(lib):
+    f = lib.fa_fwd
+    vp, i, fl = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    f.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, fl, vp]
+    f.restype = i
+    return f
+
+
+def test_status_strings(lib):
+    lib.fa_status_string.restype = ctypes.c_char_p
+    seen = set()
+    for s in range(5):
+        txt = lib.fa_status_string(s).decode()
+        assert txt and txt not in seen
+        seen.add(txt)
+    assert lib.fa_status_string(99).decode() == "unknown status"
+
+
+def test_host_validation_without_gpu(lib):
+    f = _fwd(lib)
+    p = 1 << 20   # a fake, 16-byte aligned address: never dereferenced on these paths
+    assert f(p, p + 4096, p + 8192, p + 12288, p + 16384, 1, 1, 8, 8, 64, 0, float("nan"), None) == 1
+    assert f(p, p + 4096, p + 8192, p + 12288, p + 16384, 1, 1, 8, 8, 64, 0, -0.5, None) == 1
+    assert f(p, p + 4096, p + 8192, p + 12288, p + 16384, 1, 1, 8, 8, 64, 2, 0.5, None) == 1
+    assert f(p, p + 4096, p + 8192, p + 12288, p + 16384, 1, 1, 8, 8, 96, 0, 0.5, None) == 2
+    assert f(p, p + 4096, p + 8192, p + 12288, p + 16384, -1, 1, 8, 8, 64, 0, 0.5, None) == 1
+    assert f(p, p, p + 8192, p + 12288, p + 16384, 1, 1, 8, 8, 64, 0, 0.5, None) in (1, 2, 3)
+    # empty problems are a no-op that touches nothing
+    assert f(None, None, None, None, None, 0, 4, 8, 8, 64, 0, 0.5, None) == 0
+    assert f(None, None, None, None, None, 1, 1, 0, 8, 128, 1, 0.5, None) == 0
+    # null or misaligned pointers
+    assert f(None, p, p, p, p, 1, 1, 8, 8, 64, 0, 0.5, None) == 1
+    assert f(p + 2, p + 4096, p + 8192, p + 12288, p + 16384, 1, 1, 8, 8, 64, 0, 0.5, None) == 1
+    # output overlapping an input
+    assert f(p, p + 4096, p + 8192, p + 100, p + 16384, 1, 1, 8, 8, 64, 0, 0.5, None) == 1
+
+
+def test_bwd_workspace_and_validation(lib):
+    lib.fa_bwd_workspace_bytes.argtypes = [ctypes.c_int] * 5
+    lib.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
+    ws = lib.fa_bwd_workspace_bytes(8, 32, 4096, 4096, 128)
+    rows = 8 * 32 * 4096
+    assert ws == 2 * rows * 4 + rows * 128 * 4
+    assert lib.fa_bwd_workspace_bytes(1, 1, 1, 1, 64) == 2 * 512 + 128 * 64 * 4   # rows padded to 128
+    assert lib.fa_bwd_workspace_bytes(1, 1, 8, 8, 96) == 0
+    b = lib.fa_bwd
+    vp, i, fl = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    b.argtypes = [vp] * 9 + [i] * 6 + [fl, vp, ctypes.c_size_t, vp]
+    b.restype = i
+    p = 1 << 20
+    ptrs = [p + 4096 * n for n in range(9)]
+    assert b(*ptrs, 1, 1, 8, 8, 256, 0, 0.5, p + 65536, 1 << 20, None) == 2    # d=256 backward
+    assert b(*ptrs, 1, 1, 8, 8, 64, 0, 0.5, p + 65536, 16, None) == 1          # workspace too small
+    assert b(*ptrs, 1, 1, 8, 8, 64, 0, 0.5, None, 1 << 20, None) == 1          # no workspace
+    assert b(*ptrs, 0, 1, 8, 8, 64, 0, 0.5, None, 0, None) == 0                 # empty
