@@ -1,0 +1,382 @@
+#!/usr/bin/env python
+"""Benchmark: attention fwd+bwd TFLOP/s, bf16, B8 H32 N4096 d128 causal, as a
+fraction of the GB300 dense BF16 peak.
+
+A step is one forward (fa_fwd) and one backward (fa_bwd: preprocess, tile
+loop, dQ finish) over the whole workload, inputs resident in HBM.  FLOPs per
+step: 4d (forward) + 10d (backward) per unmasked (query, key) pair, with a
+causal square counted as T^2/2 pairs per head.  Inputs (q, k, v, dO: 4 x 268 MB
+of bf16) are larger than the 129 MB L2, so no flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs under torch.distributed.run, one rank per GPU, each rank running
+the full workload on its own GPU (weak scaling, no data-path collective);
+value is the sum over ranks divided by the slowest rank's time.  Rank 0
+prints one JSON line.  --impl reference times the fp64 CPU oracle on a
+bounded sample of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention TFLOP/s fwd+bwd, bf16 B8 H32 N4096 d128 causal; % of BF16 peak"
+WORKLOAD = dict(name="attention fwd+bwd B8 H32 N4096 d128 causal", B=8, H=32, T=4096, d=128, causal=True)
+KERNELS_PER_STEP = 4   # fwd, bwd preprocess, bwd tile loop, bwd dQ finish
+
+
+# ------------------------------------------------------------------ helpers
+def flops_per_head(T: int, d: int, causal: bool) -> tuple[float, float]:
+    pairs = T * T / 2 if causal else T * T
+    return 4.0 * d * pairs, 10.0 * d * pairs
+
+
+def step_flops(w=WORKLOAD) -> tuple[float, float]:
+    f, b = flops_per_head(w["T"], w["d"], w["causal"])
+    n = w["B"] * w["H"]
+    return f * n, b * n
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return {"bf16_tflops": float(p["bf16_tflops"]), "bf16_tflops_sustained": float(p["bf16_tflops_sustained"]),
+                "hbm_gbs": float(p["hbm_gbs"]), "source": "measured"}
+    except Exception:
+        return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def dist_info():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Max over ranks (a host-side reduction of timings, not a data-path collective)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu), "-lms", "50"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(self.REASONS, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU oracle leg
+def oracle_sample(min_seconds: float = 10.0, max_heads: int = 64) -> dict:
+    """The fp64 oracle (as it stands) on whole heads of the workload: forward for every
+    row, backward for every row and key.  Runs heads until min_seconds have passed."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from exact_io_aware_05_gb300 import inputs
+
+    w = WORKLOAD
+    wl = inputs.small(1, 1, w["T"], w["T"], w["d"], w["causal"], seed=4, scale=1.0 / math.sqrt(w["d"]),
+                      backward=True)
+    cores = oracle.default_threads()
+    f_head, b_head = flops_per_head(w["T"], w["d"], w["causal"])
+    heads, t_total = 0, 0.0
+    while heads < max_heads and (t_total < min_seconds or heads == 0):
+        x = inputs.generate(inputs.replace(wl, seed=4 + heads))
+        q, k, v, do = (x[n][0, 0].to(torch.float64).numpy() for n in ("q", "k", "v", "do"))
+        t0 = time.perf_counter()
+        oracle.attention_fwd(q, k, v, wl.causal, wl.scale, nthreads=cores)
+        oracle.attention_bwd(q, k, v, do, wl.causal, wl.scale, nthreads=cores)
+        t_total += time.perf_counter() - t0
+        heads += 1
+    tflops = heads * (f_head + b_head) / t_total / 1e12
+    return {"value": tflops, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{heads} of the {w['B'] * w['H']} heads (T={w['T']}, d={w['d']}, causal), forward every row "
+                      f"+ backward every row and key, fp64, {t_total:.1f} s",
+            "seconds": t_total}
+
+
+def run_reference(args) -> None:
+    rank, _, world = dist_info()
+    if rank != 0:
+        return
+    import torch  # noqa: F401  (inputs module uses torch's CPU generator)
+
+    import oracle
+    from exact_io_aware_05_gb300 import inputs
+
+    w = WORKLOAD
+    wl = inputs.small(1, 1, w["T"], w["T"], w["d"], w["causal"], seed=4, scale=1.0 / math.sqrt(w["d"]),
+                      backward=True)
+    cores = oracle.default_threads()
+    f_head, b_head = flops_per_head(w["T"], w["d"], w["causal"])
+    x = inputs.generate(wl)
+    import numpy as np  # noqa: F401
+    q, k, v, do = (x[n][0, 0].to(torch.float64).numpy() for n in ("q", "k", "v", "do"))
+
+    def one_step():
+        oracle.attention_fwd(q, k, v, wl.causal, wl.scale, nthreads=cores)
+        oracle.attention_bwd(q, k, v, do, wl.causal, wl.scale, nthreads=cores)
+
+    for _ in range(args.warmup):
+        one_step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one_step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = (f_head + b_head) / dt / 1e12
+    sample = f"one head (T={w['T']}, d={w['d']}, causal) per step: forward every row + backward every row and key"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_block(world),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_block(world: int) -> dict:
+    w = WORKLOAD
+    return {"workload": w["name"], "B": w["B"], "H": w["H"], "N": w["T"], "d": w["d"], "causal": w["causal"],
+            "flops": "4d fwd + 10d bwd per unmasked pair; causal square = T^2/2 pairs",
+            "l2": "no flush: inputs q,k,v,dO = 4 x 268 MB bf16, larger than the 129 MB L2",
+            "parallelism": f"replicas x{world} (one full workload per GPU, no data-path collective)"}
+
+
+# ------------------------------------------------------------------ GPU leg
+def run_ours(args) -> None:
+    import torch
+
+    rank, local, world = dist_info()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    from exact_io_aware_05_gb300 import fa
+
+    w = WORKLOAD
+    B, H, T, d, causal = w["B"], w["H"], w["T"], w["d"], w["causal"]
+    scale = 1.0 / math.sqrt(d)
+    g = torch.Generator(device=dev)
+    g.manual_seed(1234 + rank)
+    shp = (B, H, T, d)
+    q, k, v, do = (torch.randn(shp, device=dev, generator=g).to(torch.bfloat16) for _ in range(4))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, T), device=dev, dtype=torch.float32)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = fa.alloc_workspace(B, H, T, T, d, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        fa.fa_fwd(q, k, v, o, lse, causal, scale, stream)
+        if evs is not None:
+            evs[1].record(stream)
+        fa.fa_bwd_stage(1, q, k, v, o, lse, do, dq, dk, dv, causal, scale, ws, stream)
+        if evs is not None:
+            evs[2].record(stream)
+        fa.fa_bwd_stage(2, q, k, v, o, lse, do, dq, dk, dv, causal, scale, ws, stream)
+        if evs is not None:
+            evs[3].record(stream)
+        fa.fa_bwd_stage(3, q, k, v, o, lse, do, dq, dk, dv, causal, scale, ws, stream)
+        if evs is not None:
+            evs[4].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    if fa.fa_sync_status(stream) != fa.FA_OK:
+        raise RuntimeError("device status error during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local) if rank == 0 else None
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)   # let the sampler attach before the timed region
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if sampler else None
+    st = fa.fa_sync_status(stream)
+    if st != fa.FA_OK:
+        raise RuntimeError(f"device status {st} after the timed region")
+
+    total_ms = t_start.elapsed_time(t_end)
+    ms_step = reduce_max(total_ms / args.steps, world, dev)
+    per = [[e[i].elapsed_time(e[i + 1]) for i in range(4)] for e in evs]
+    fwd_ms = statistics.mean(p[0] for p in per)
+    pre_ms = statistics.mean(p[1] for p in per)
+    main_ms = statistics.mean(p[2] for p in per)
+    dq_ms = statistics.mean(p[3] for p in per)
+    f_fwd, f_bwd = step_flops()
+    value = world * (f_fwd + f_bwd) / (ms_step * 1e-3) / 1e12
+    peaks = measured_peaks()
+    peak = peaks["bf16_tflops"]
+    fwd_tf = f_fwd / (fwd_ms * 1e-3) / 1e12
+    main_tf = f_bwd / (main_ms * 1e-3) / 1e12
+    bwd_tf = f_bwd / ((pre_ms + main_ms + dq_ms) * 1e-3) / 1e12
+    dom = ("bwd_main", main_tf) if main_ms >= fwd_ms else ("fwd", fwd_tf)
+
+    # e2e: the public API with host buffers, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        pin = {n: t.to("cpu").pin_memory() for n, t in (("q", q), ("k", k), ("v", v), ("do", do))}
+        outs = {n: torch.empty(shp, dtype=torch.bfloat16).pin_memory() for n in ("o", "dq", "dk", "dv")}
+        out_lse = torch.empty((B, H, T), dtype=torch.float32).pin_memory()
+        dbuf = {n: torch.empty(shp, device=dev, dtype=torch.bfloat16) for n in ("q", "k", "v", "do")}
+
+        def e2e_step():
+            for n in ("q", "k", "v", "do"):
+                dbuf[n].copy_(pin[n], non_blocking=True)
+            fa.fa_fwd(dbuf["q"], dbuf["k"], dbuf["v"], o, lse, causal, scale, stream)
+            fa.fa_bwd(dbuf["q"], dbuf["k"], dbuf["v"], o, lse, dbuf["do"], dq, dk, dv, causal, scale, ws, stream)
+            outs["o"].copy_(o, non_blocking=True)
+            out_lse.copy_(lse, non_blocking=True)
+            outs["dq"].copy_(dq, non_blocking=True)
+            outs["dk"].copy_(dk, non_blocking=True)
+            outs["dv"].copy_(dv, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        n_e2e = max(3, min(args.steps, 10))
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            torch.distributed.barrier()
+        a0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        a1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = reduce_max(a0.elapsed_time(a1) / n_e2e, world, dev)
+        h2d = sum(t.numel() * t.element_size() for t in pin.values())
+        d2h = sum(t.numel() * t.element_size() for t in outs.values()) + out_lse.numel() * 4
+        e2e = {"value": world * (f_fwd + f_bwd) / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+               "api": "fa_fwd + fa_bwd with pinned host buffers"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb = oracle_sample(min_seconds=args.cpu_seconds)
+        cpu = {k_: cb[k_] for k_ in ("value", "unit", "cores", "kind", "sample")}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_block(world),
+        "pct_of_bf16_peak": 100.0 * value / world / peak,
+        "passes": {"fwd": {"ms": fwd_ms, "tflops": fwd_tf, "pct_of_peak": 100 * fwd_tf / peak},
+                   "bwd": {"ms": pre_ms + main_ms + dq_ms, "tflops": bwd_tf, "pct_of_peak": 100 * bwd_tf / peak,
+                           "preprocess_ms": pre_ms, "tile_loop_ms": main_ms, "dq_finish_ms": dq_ms}},
+        "roofline": {"kernel": dom[0], "bound": "tensor", "achieved": dom[1], "peak": peak, "unit": "TFLOP/s",
+                     "frac": dom[1] / peak, "traffic": None,
+                     "peak_source": f"{peaks['source']} bf16 (burst), MEASURED_PEAKS.json"},
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+    if dist_info()[2] > 1:
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -235,9 +235,9 @@ size_t fa_bwd_workspace_bytes(int B, int H, int Tq, int Tk, int d)
     return fa::bwd_workspace_bytes(B * H, Tq, d);
 }
 
-int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dO, void *dq,
-           void *dk, void *dv, int B, int H, int Tq, int Tk, int d, int causal, float scale, void *workspace,
-           size_t workspace_bytes, fa_stream_t stream)
+static int bwd_common(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dO,
+                      void *dq, void *dk, void *dv, int B, int H, int Tq, int Tk, int d, int causal, float scale,
+                      void *workspace, size_t workspace_bytes, int stages, fa_stream_t stream)
 {
     int st = fa::check_sizes(B, H, Tq, Tk, d, causal, scale);
     if (st != fa::OK)
@@ -273,7 +273,25 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
         return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const fa::BwdWorkspace ws = fa::bwd_workspace_carve(workspace, (int)bh, Tq, d);
-    return fa::bwd_launch(q, k, v, o, lse, dO, dq, dk, dv, (int)bh, Tq, Tk, d, causal, scale, ws, s);
+    return fa::bwd_launch(q, k, v, o, lse, dO, dq, dk, dv, (int)bh, Tq, Tk, d, causal, scale, ws, stages, s);
+}
+
+int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dO, void *dq,
+           void *dk, void *dv, int B, int H, int Tq, int Tk, int d, int causal, float scale, void *workspace,
+           size_t workspace_bytes, fa_stream_t stream)
+{
+    return bwd_common(q, k, v, o, lse, dO, dq, dk, dv, B, H, Tq, Tk, d, causal, scale, workspace, workspace_bytes, 7,
+                      stream);
+}
+
+int fa_bwd_stage(int stage, const void *q, const void *k, const void *v, const void *o, const float *lse,
+                 const void *dO, void *dq, void *dk, void *dv, int B, int H, int Tq, int Tk, int d, int causal,
+                 float scale, void *workspace, size_t workspace_bytes, fa_stream_t stream)
+{
+    if (stage < 1 || stage > 3)
+        return FA_ERR_INVALID_ARG;
+    return bwd_common(q, k, v, o, lse, dO, dq, dk, dv, B, H, Tq, Tk, d, causal, scale, workspace, workspace_bytes,
+                      1 << (stage - 1), stream);
 }
 
 int fa_sync_status(fa_stream_t stream)

@@ -1,22 +1,711 @@
-// fa_bwd_sm103.cu -- backward pass (placeholder until the tcgen05 kernels land).
+// fa_bwd_sm103.cu -- backward pass of IO-aware exact attention on sm_103a.
+//
+// What it computes (zerotofrontier.app "FlashAttention", Efficient attention
+// 12.3, section "The backward pass, derived"), with c the softmax scale:
+//   preprocess   D_r = dO_r . O_r                       (observation 2)
+//   per tile     P_ij = exp(c S_ij - lse_i)             (observation 1, S_ij = Q_i K_j^T)
+//                dV_j += P_ij^T dO_i,  dP_ij = dO_i V_j^T,  dS_ij = P_ij o (dP_ij - D_i)
+//                dK_j += c dS_ij^T Q_i,  dQ_i += c dS_ij K_j      (observation 3)
+// with the key blocks outside: dK_j and dV_j accumulate on chip and are
+// written once, dQ_i is accumulated in HBM by fp32 atomic additions ("Which
+// loop goes outside?").  Causal tiles wholly above the diagonal are skipped,
+// exactly as in the forward pass.  Five tile products per tile ("The price of
+// recomputation").
+//
+// GB300 design:
+//   * three kernels on one stream: bwd_pre (D, log2-domain lse, dQ accumulator
+//     zeroed), bwd_main (the tile loop below), bwd_dq (scale and round dQ);
+//   * bwd_main is persistent; a unit is one 128-key block of one head, taken
+//     longest-first within groups of heads;
+//   * warp 0 streams K_j, V_j once per unit and Q_i, dO_i, lse_i, D_i per query
+//     block through a 3-stage ring (TMA tiles + bulk copies); warp 1 issues all
+//     tcgen05.mma; two softmax warpgroups each rebuild half of a tile's
+//     P^T and dS^T from S^T and dP^T in tensor memory; a fourth warpgroup
+//     drains dQ from tensor memory into the fp32 accumulator with atomic adds
+//     and writes dK, dV at the end of the unit;
+//   * tensor memory: S^T and dP^T (128 keys x BQ queries), two dQ buffers, and
+//     the dV, dK accumulators.  For d = 128 the query block is 64 rows and dQ
+//     is formed transposed (dQ^T = K_j^T dS^T, M = d) so that every region fits
+//     in 512 columns; for d = 64 the query block is 128 rows and dQ = dS K_j;
+//   * the dQ product of block g is issued after the S/dP products of block
+//     g+1, so the tensor core works while the softmax warpgroups run;
+//   * every MMA that overwrites a tensor-memory region waits for the MMA that
+//     last read it as an operand, and every wait is bounded.
 #include "fa_common.cuh"
 #include "fa_internal.h"
 
 namespace fa {
 
-__device__ int g_bwd_status;
+__device__ int g_bwd_status;   // device status word of the backward kernels
 
-int bwd_launch(const void *, const void *, const void *, const void *, const float *, const void *, void *, void *,
-               void *, int, int, int, int, int, float, const BwdWorkspace &, cudaStream_t)
+namespace {
+
+constexpr int BK = 128;   // keys per unit (= MMA M for S^T, dP^T, dV, dK)
+constexpr int NST = 3;    // Q/dO stages
+
+template <int D>
+struct BwdCfg;
+template <>
+struct BwdCfg<64> {
+    static constexpr int BQ = 128;       // queries per block
+    static constexpr bool DQT = false;   // dQ = dS K_j (M = queries)
+};
+template <>
+struct BwdCfg<128> {
+    static constexpr int BQ = 64;
+    static constexpr bool DQT = true;    // dQ^T = K_j^T dS^T (M = d)
+};
+
+template <int D>
+struct BwdLayout {
+    static constexpr int BQ = BwdCfg<D>::BQ;
+    static constexpr bool DQT = BwdCfg<D>::DQT;
+    static constexpr int KCH = D / 64;
+    static constexpr int KV_CHUNK = BK * 128;            // one 64-column chunk of K_j or V_j
+    static constexpr int KV_TILE = KCH * KV_CHUNK;
+    static constexpr int Q_CHUNK = BQ * 128;
+    static constexpr int Q_TILE = KCH * Q_CHUNK;
+    static constexpr int DS_CHUNK = BK * 128;            // dS^T: 128 keys x 64 queries bf16
+    static constexpr int DS_TILE = (BQ / 64) * DS_CHUNK;
+    // stage: Q_i, dO_i, lse2_i, D_i
+    static constexpr int ST_Q = 0, ST_DO = Q_TILE, ST_LSE = 2 * Q_TILE, ST_D = 2 * Q_TILE + BQ * 4;
+    static constexpr int ST_BYTES = ((2 * Q_TILE + 2 * BQ * 4) + 1023) / 1024 * 1024;
+    static constexpr int OFF_K = 0, OFF_V = KV_TILE, OFF_ST = 2 * KV_TILE;
+    static constexpr int OFF_DS = OFF_ST + NST * ST_BYTES;
+    static constexpr int OFF_BAR = OFF_DS + 2 * DS_TILE;
+    enum : int {
+        B_KVFULL = 0, B_KVEMPTY, B_STFULL, B_STEMPTY = B_STFULL + NST, B_SFULL = B_STEMPTY + NST,
+        B_PFULL, B_DVDONE, B_DKDONE, B_DQFULL, B_DQEMPTY = B_DQFULL + 2, B_DKVFULL = B_DQEMPTY + 2,
+        B_DKVEMPTY, B_DRAIN, NBAR
+    };
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+    // tensor memory columns
+    static constexpr int T_S = 0, T_DP = BQ;
+    static constexpr int T_DQ = DQT ? 2 * BQ : 256 + 2 * D;     // two buffers of DQ_COLS
+    static constexpr int DQ_COLS = DQT ? BQ : D;
+    static constexpr int T_DV = DQT ? 2 * BQ + 2 * DQ_COLS : 256, T_DK = T_DV + D;
+    static constexpr int TMEM_COLS = 512;
+    static_assert(T_DK + D <= TMEM_COLS && T_DQ + 2 * DQ_COLS <= TMEM_COLS, "tensor memory budget");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+    static constexpr int NTHREADS = 512;
+    // instruction descriptors
+    static constexpr uint32_t ID_SDP = idesc_bf16_f32(128, BQ, false, false);   // K_j Q_i^T, V_j dO_i^T
+    static constexpr uint32_t ID_DKV = idesc_bf16_f32(128, D, false, true);     // P^T dO_i, dS^T Q_i
+    static constexpr uint32_t ID_DQ = DQT ? idesc_bf16_f32(128, BQ, true, true)   // K_j^T dS^T
+                                          : idesc_bf16_f32(128, D, true, true);   // dS K_j
+};
+
+enum WaitSite : int {
+    SITE_P_KVEMPTY = 1, SITE_P_STEMPTY, SITE_M_KVFULL, SITE_M_STFULL, SITE_M_DVDONE, SITE_M_DKDONE,
+    SITE_M_PFULL, SITE_M_DKVEMPTY, SITE_M_DQEMPTY, SITE_S_SFULL, SITE_D_DQFULL, SITE_D_DKVFULL
+};
+
+struct BwdArgs {
+    const float *lse2, *delta;
+    float *dq_acc;
+    __nv_bfloat16 *dk, *dv;
+    int BH, Tq, Tk, Tq_pad, causal;
+    float scale, scale_log2;
+    int nkb, units, group;
+    uint64_t timeout_ns;
+};
+
+struct Unit {
+    int bh, j;     // head, key block
+    int i0, nq;    // first query block, number of query blocks
+};
+
+template <int D>
+__device__ __forceinline__ Unit make_unit(int u, const BwdArgs &a)
 {
-    return ERR_UNSUPPORTED;
+    using L = BwdLayout<D>;
+    const int per_group = a.group * a.nkb;
+    const int g = u / per_group;
+    const int w = u - g * per_group;
+    const int heads_here = min(a.group, a.BH - g * a.group);
+    const int lvl = w / heads_here;            // key block: smaller blocks see more queries (causal)
+    Unit x;
+    x.bh = g * a.group + (w - lvl * heads_here);
+    x.j = lvl;
+    const int nqb = (a.Tq + L::BQ - 1) / L::BQ;
+    int first_row = 0;
+    if (a.causal) {
+        const long r = (long)x.j * BK - (a.Tk - a.Tq);   // first query that sees key j*BK
+        first_row = r < 0 ? 0 : (int)min(r, (long)a.Tq);
+    }
+    x.i0 = first_row / L::BQ;
+    x.nq = nqb - x.i0;
+    if (x.nq < 0)
+        x.nq = 0;
+    return x;
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(512, 1)
+    bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const BwdArgs a)
+{
+    using L = BwdLayout<D>;
+    constexpr int BQ = L::BQ;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (sbase - raw);
+    const uint32_t bar0 = sbase + L::OFF_BAR;
+    auto bar = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
+    const uint32_t warp = warp_id(), lane = lane_id();
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(L::B_KVFULL), 1);
+        mbar_init(bar(L::B_KVEMPTY), 1);
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(bar(L::B_STFULL + s), 1);
+            mbar_init(bar(L::B_STEMPTY + s), 1);
+        }
+        mbar_init(bar(L::B_SFULL), 1);
+        mbar_init(bar(L::B_PFULL), 256);
+        mbar_init(bar(L::B_DVDONE), 1);
+        mbar_init(bar(L::B_DKDONE), 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(L::B_DQFULL + b), 1);
+            mbar_init(bar(L::B_DQEMPTY + b), 128);
+        }
+        mbar_init(bar(L::B_DKVFULL), 1);
+        mbar_init(bar(L::B_DKVEMPTY), 128);
+        mbar_init(bar(L::B_DRAIN), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        tma_prefetch_desc(&tm_do);
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), L::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtx ctx{abort_flag, &g_bwd_status, a.timeout_ns};
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint64_t pol_keep = policy_evict_last();
+            uint32_t n_kv = 0, n_st = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+                const Unit x = make_unit<D>(u, a);
+                if (x.nq == 0)
+                    continue;
+                if (n_kv > 0 && !mbar_wait(bar(L::B_KVEMPTY), (n_kv - 1) & 1, ctx, SITE_P_KVEMPTY))
+                    break;
+                mbar_arrive_expect_tx(bar(L::B_KVFULL), 2 * L::KV_TILE);
+                for (int c = 0; c < L::KCH; ++c) {
+                    tma_load_3d(sbase + L::OFF_K + c * L::KV_CHUNK, &tm_k, bar(L::B_KVFULL), c * 64, x.j * BK, x.bh);
+                    tma_load_3d(sbase + L::OFF_V + c * L::KV_CHUNK, &tm_v, bar(L::B_KVFULL), c * 64, x.j * BK, x.bh);
+                }
+                ++n_kv;
+                for (int i = x.i0; i < x.i0 + x.nq; ++i) {
+                    const uint32_t s = n_st % NST;
+                    if (n_st >= NST && !mbar_wait(bar(L::B_STEMPTY + s), ((n_st / NST) - 1) & 1, ctx, SITE_P_STEMPTY)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t st = sbase + L::OFF_ST + s * L::ST_BYTES;
+                    mbar_arrive_expect_tx(bar(L::B_STFULL + s), 2 * L::Q_TILE + 2 * BQ * 4);
+                    for (int c = 0; c < L::KCH; ++c) {
+                        tma_load_3d_hint(st + L::ST_Q + c * L::Q_CHUNK, &tm_q, bar(L::B_STFULL + s), c * 64, i * BQ,
+                                         x.bh, pol_keep);
+                        tma_load_3d_hint(st + L::ST_DO + c * L::Q_CHUNK, &tm_do, bar(L::B_STFULL + s), c * 64,
+                                         i * BQ, x.bh, pol_keep);
+                    }
+                    const size_t roff = (size_t)x.bh * a.Tq_pad + (size_t)i * BQ;
+                    bulk_load(st + L::ST_LSE, a.lse2 + roff, BQ * 4, bar(L::B_STFULL + s));
+                    bulk_load(st + L::ST_D, a.delta + roff, BQ * 4, bar(L::B_STFULL + s));
+                    ++n_st;
+                }
+            }
+            // drain copies in flight
+            const uint32_t lo = n_st > (uint32_t)NST ? n_st - NST : 0;
+            for (uint32_t i = lo; i < n_st; ++i)
+                mbar_wait_drain(bar(L::B_STFULL + i % NST), (i / NST) & 1, a.timeout_ns);
+            if (n_kv > 0)
+                mbar_wait_drain(bar(L::B_KVFULL), (n_kv - 1) & 1, a.timeout_ns);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t g = 0, nu = 0;   // global query-block and unit counters of this CTA
+            bool ok = true;
+            const uint32_t k_s = sbase + L::OFF_K, v_s = sbase + L::OFF_V;
+            auto issue_dq = [&](uint32_t gq) -> bool {
+                const uint32_t b = gq & 1;
+                if (gq >= 2 && !mbar_wait(bar(L::B_DQEMPTY + b), ((gq - 2) >> 1) & 1, ctx, SITE_M_DQEMPTY))
+                    return false;
+                tc_fence_after();
+                const uint32_t ds = sbase + L::OFF_DS + b * L::DS_TILE;
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk) {
+                    uint64_t ad, bd;
+                    if constexpr (L::DQT) {
+                        // A = K_j^T (M = d, MN-major), B = dS^T (N = queries, MN-major)
+                        ad = sdesc_sw128(k_s + kk * 2048, L::KV_CHUNK, 1024);
+                        bd = sdesc_sw128(ds + kk * 2048, L::DS_CHUNK, 1024);
+                    } else {
+                        // A = dS (M = queries, MN-major), B = K_j (N = d, MN-major)
+                        ad = sdesc_sw128(ds + kk * 2048, L::DS_CHUNK, 1024);
+                        bd = sdesc_sw128(k_s + kk * 2048, L::KV_CHUNK, 1024);
+                    }
+                    mma_ss(tmem + L::T_DQ + b * L::DQ_COLS, ad, bd, L::ID_DQ, kk > 0 ? 1u : 0u);
+                }
+                tc_commit(bar(L::B_DQFULL + b));
+                return true;
+            };
+            for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+                const Unit x = make_unit<D>(u, a);
+                if (x.nq == 0)
+                    continue;
+                if (!mbar_wait(bar(L::B_KVFULL), nu & 1, ctx, SITE_M_KVFULL))
+                    break;
+                for (int i = 0; i < x.nq; ++i, ++g) {
+                    const uint32_t s = g % NST;
+                    if (!mbar_wait(bar(L::B_STFULL + s), (g / NST) & 1, ctx, SITE_M_STFULL)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t st = sbase + L::OFF_ST + s * L::ST_BYTES;
+                    // S^T = K_j Q_i^T overwrites P^T of the previous block: dV(g-1) must be done
+                    if (g > 0 && !mbar_wait(bar(L::B_DVDONE), (g - 1) & 1, ctx, SITE_M_DVDONE)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk & 3) * 32;
+                        mma_ss(tmem + L::T_S, sdesc_sw128(k_s + (kk >> 2) * L::KV_CHUNK + off, 16, 1024),
+                               sdesc_sw128(st + L::ST_Q + (kk >> 2) * L::Q_CHUNK + off, 16, 1024), L::ID_SDP,
+                               kk > 0 ? 1u : 0u);
+                    }
+                    // dP^T = V_j dO_i^T overwrites dS^T of the previous block: dK(g-1) must be done
+                    if (g > 0 && !mbar_wait(bar(L::B_DKDONE), (g - 1) & 1, ctx, SITE_M_DKDONE)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk & 3) * 32;
+                        mma_ss(tmem + L::T_DP, sdesc_sw128(v_s + (kk >> 2) * L::KV_CHUNK + off, 16, 1024),
+                               sdesc_sw128(st + L::ST_DO + (kk >> 2) * L::Q_CHUNK + off, 16, 1024), L::ID_SDP,
+                               kk > 0 ? 1u : 0u);
+                    }
+                    tc_commit(bar(L::B_SFULL));
+                    // dQ of the previous block of this unit runs while the softmax works
+                    if (i > 0 && !issue_dq(g - 1)) {
+                        ok = false;
+                        break;
+                    }
+                    if (!mbar_wait(bar(L::B_PFULL), g & 1, ctx, SITE_M_PFULL)) {
+                        ok = false;
+                        break;
+                    }
+                    if (i == 0 && nu > 0 && !mbar_wait(bar(L::B_DKVEMPTY), (nu - 1) & 1, ctx, SITE_M_DKVEMPTY)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    // dV_j += P^T dO_i ; dK_j += dS^T Q_i  (A from tensor memory, B MN-major)
+#pragma unroll
+                    for (int kk = 0; kk < BQ / 16; ++kk) {
+                        // P^T / dS^T of query columns [16kk, 16kk+16): each softmax warpgroup
+                        // packs its half of the columns at the start of its half of the region
+                        const uint32_t col = (kk < BQ / 32) ? kk * 8 : BQ / 2 + (kk - BQ / 32) * 8;
+                        const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+                        mma_ts(tmem + L::T_DV, tmem + L::T_S + col,
+                               sdesc_sw128(st + L::ST_DO + kk * 2048, L::Q_CHUNK, 1024), L::ID_DKV, acc);
+                    }
+                    tc_commit(bar(L::B_DVDONE));
+#pragma unroll
+                    for (int kk = 0; kk < BQ / 16; ++kk) {
+                        const uint32_t col = (kk < BQ / 32) ? kk * 8 : BQ / 2 + (kk - BQ / 32) * 8;
+                        const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+                        mma_ts(tmem + L::T_DK, tmem + L::T_DP + col,
+                               sdesc_sw128(st + L::ST_Q + kk * 2048, L::Q_CHUNK, 1024), L::ID_DKV, acc);
+                    }
+                    tc_commit(bar(L::B_DKDONE));
+                    tc_commit(bar(L::B_STEMPTY + s));
+                    if (i == x.nq - 1) {
+                        if (!issue_dq(g)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_commit(bar(L::B_DKVFULL));
+                        tc_commit(bar(L::B_KVEMPTY));
+                    }
+                }
+                ++nu;
+            }
+            tc_commit(bar(L::B_DRAIN));
+            mbar_wait_drain(bar(L::B_DRAIN), 0, a.timeout_ns);
+        }
+        __syncwarp();
+    } else if (warp >= 4 && warp < 12) {
+        // ------------------------------------------------------------ softmax (two warpgroups)
+        const int half = (int)(warp - 4) >> 2;          // query columns [half*BQ/2, (half+1)*BQ/2)
+        const uint32_t quarter = warp & 3u;
+        const int key_in_blk = (int)(quarter * 32 + lane);
+        const uint32_t lane_base = tmem + ((quarter * 32u) << 16);
+        constexpr int HC = BQ / 2;                      // columns per thread
+        uint32_t g = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+            const Unit x = make_unit<D>(u, a);
+            const int l = x.j * BK + key_in_blk;         // this thread's key
+            for (int i = 0; i < x.nq; ++i, ++g) {
+                if (!mbar_wait(bar(L::B_SFULL), g & 1, ctx, SITE_S_SFULL)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t s = g % NST;
+                const float *lse2 = reinterpret_cast<const float *>(smem + L::OFF_ST + s * L::ST_BYTES + L::ST_LSE);
+                const float *dl = reinterpret_cast<const float *>(smem + L::OFF_ST + s * L::ST_BYTES + L::ST_D);
+                const int qb = (x.i0 + i) * BQ;                   // first query row of the block
+                // causal: column q is allowed iff qb + q >= l - (Tk - Tq)
+                int qmin = 0;
+                if (a.causal) {
+                    const long lim = (long)l - (a.Tk - a.Tq) - qb;
+                    qmin = (int)max(0L, min((long)BQ, lim));
+                }
+                uint8_t *ds_row = smem + L::OFF_DS + (g & 1) * L::DS_TILE + key_in_blk * 128;
+#pragma unroll
+                for (int c = 0; c < HC / 32; ++c) {
+                    const int q0 = half * HC + c * 32;          // first query column of this chunk
+                    uint32_t sv[32], dv[32];
+                    tmem_ld_x32(lane_base + L::T_S + q0, sv);
+                    tmem_ld_x32(lane_base + L::T_DP + q0, dv);
+                    uint32_t pk[16], dk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        float pr[2], dsv[2];
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int q = q0 + 2 * e + h;
+                            float p = ex2_approx(fmaf(__uint_as_float(sv[2 * e + h]), a.scale_log2, -lse2[q]));
+                            p = (q >= qmin) ? p : 0.f;
+                            pr[h] = p;
+                            dsv[h] = p * (__uint_as_float(dv[2 * e + h]) - dl[q]);
+                        }
+                        pk[e] = pack_bf16x2(pr[0], pr[1]);
+                        dk[e] = pack_bf16x2(dsv[0], dsv[1]);
+                    }
+                    // P^T and dS^T (bf16) over the first half of this warpgroup's columns
+                    const uint32_t tcol = half * HC + c * 16;
+                    tmem_st_x16(lane_base + L::T_S + tcol, pk);
+                    tmem_st_x16(lane_base + L::T_DP + tcol, dk);
+                    // dS^T row of this key into shared memory: [key][query] with 128-byte
+                    // swizzle, 64 queries per 128-byte row chunk
+                    uint8_t *chunk = ds_row + (q0 / 64) * L::DS_CHUNK;
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4) {
+                        const int unit16 = ((q0 % 64) / 8) + v4;
+                        const int sw = unit16 ^ (key_in_blk & 7);
+                        *reinterpret_cast<uint4 *>(chunk + sw * 16) =
+                            make_uint4(dk[4 * v4], dk[4 * v4 + 1], dk[4 * v4 + 2], dk[4 * v4 + 3]);
+                    }
+                }
+                tmem_wait_st();
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(bar(L::B_PFULL));
+            }
+        }
+    } else if (warp >= 12) {
+        // ------------------------------------------------------------ dQ drain + dK/dV epilogue
+        const uint32_t quarter = warp & 3u;
+        const int row = (int)(quarter * 32 + lane);      // TMEM lane
+        const uint32_t lane_base = tmem + ((quarter * 32u) << 16);
+        uint32_t g = 0, nu = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+            const Unit x = make_unit<D>(u, a);
+            const int l = x.j * BK + row;
+            const size_t krow = (size_t)x.bh * a.Tk + l;
+            if (x.nq == 0) {
+                if (l < a.Tk) {
+                    uint4 *pk_ = reinterpret_cast<uint4 *>(a.dk + krow * D);
+                    uint4 *pv_ = reinterpret_cast<uint4 *>(a.dv + krow * D);
+                    for (int e = 0; e < D / 8; ++e) {
+                        pk_[e] = make_uint4(0, 0, 0, 0);
+                        pv_[e] = make_uint4(0, 0, 0, 0);
+                    }
+                }
+                continue;
+            }
+            for (int i = 0; i < x.nq; ++i, ++g) {
+                const uint32_t b = g & 1;
+                if (!mbar_wait(bar(L::B_DQFULL + b), (g >> 1) & 1, ctx, SITE_D_DQFULL)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const int qb = (x.i0 + i) * BQ;
+                float *acc = a.dq_acc + ((size_t)x.bh * a.Tq_pad + qb) * D;
+#pragma unroll
+                for (int c = 0; c < L::DQ_COLS / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld_x32(lane_base + L::T_DQ + b * L::DQ_COLS + c * 32, v);
+                    if constexpr (L::DQT) {
+                        // lane = feature, column = query: a warp adds 32 consecutive floats per query
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            atomicAdd(acc + (size_t)(c * 32 + e) * D + row, __uint_as_float(v[e]));
+                    } else {
+                        // lane = query, column = feature
+                        float4 *dst = reinterpret_cast<float4 *>(acc + (size_t)row * D + c * 32);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            atomicAdd(dst + e, make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                                                           __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3])));
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(bar(L::B_DQEMPTY + b));
+            }
+            if (!ok)
+                break;
+            if (!mbar_wait(bar(L::B_DKVFULL), nu & 1, ctx, SITE_D_DKVFULL))
+                break;
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t v[32], w[16];
+                tmem_ld_x32(lane_base + L::T_DV + c * 32, v);
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    w[e] = pack_bf16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+                if (l < a.Tk) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(a.dv + krow * D + c * 32);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+                }
+                tmem_ld_x32(lane_base + L::T_DK + c * 32, v);
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    w[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * a.scale, __uint_as_float(v[2 * e + 1]) * a.scale);
+                if (l < a.Tk) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(a.dk + krow * D + c * 32);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bar(L::B_DKVEMPTY));
+            ++nu;
+        }
+    }
+    // ------------------------------------------------------------ teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, L::TMEM_COLS);
+    }
+}
+
+// D_r = dO_r . O_r, lse in log2 units (+inf where no key is allowed or past Tq),
+// and the fp32 dQ accumulator zeroed.  One warp per (padded) row.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__restrict__ o,
+                                                      const __nv_bfloat16 *__restrict__ dO,
+                                                      const float *__restrict__ lse, float *__restrict__ lse2,
+                                                      float *__restrict__ delta, float *__restrict__ dq_acc, int BH,
+                                                      int Tq, int Tq_pad)
+{
+    const size_t rows = (size_t)BH * Tq_pad;
+    const int lane = threadIdx.x & 31;
+    for (size_t gr = (blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5; gr < rows;
+         gr += ((size_t)gridDim.x * blockDim.x) >> 5) {
+        const size_t bh = gr / Tq_pad;
+        const int r = (int)(gr - bh * Tq_pad);
+        float dsum = 0.f;
+        if (r < Tq) {
+            const size_t src = (bh * Tq + r) * D;
+            constexpr int PER = D / 32;   // elements per lane (2 or 4)
+            if constexpr (PER == 4) {
+                const uint2 ov = *reinterpret_cast<const uint2 *>(o + src + lane * 4);
+                const uint2 gv = *reinterpret_cast<const uint2 *>(dO + src + lane * 4);
+                const __nv_bfloat162 *o2 = reinterpret_cast<const __nv_bfloat162 *>(&ov);
+                const __nv_bfloat162 *g2 = reinterpret_cast<const __nv_bfloat162 *>(&gv);
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float2 a2 = __bfloat1622float2(o2[e]), b2 = __bfloat1622float2(g2[e]);
+                    dsum = fmaf(a2.x, b2.x, dsum);
+                    dsum = fmaf(a2.y, b2.y, dsum);
+                }
+            } else {
+                const __nv_bfloat162 ov = *reinterpret_cast<const __nv_bfloat162 *>(o + src + lane * 2);
+                const __nv_bfloat162 gv = *reinterpret_cast<const __nv_bfloat162 *>(dO + src + lane * 2);
+                const float2 a2 = __bfloat1622float2(ov), b2 = __bfloat1622float2(gv);
+                dsum = fmaf(a2.x, b2.x, dsum);
+                dsum = fmaf(a2.y, b2.y, dsum);
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+                dsum += __shfl_xor_sync(0xffffffffu, dsum, off);
+        }
+        if (lane == 0) {
+            float l2 = INFINITY;
+            if (r < Tq) {
+                const float lv = lse[bh * Tq + r];
+                l2 = (lv == -INFINITY) ? INFINITY : lv * 1.4426950408889634f;
+            }
+            lse2[gr] = l2;
+            delta[gr] = r < Tq ? dsum : 0.f;
+        }
+        float4 *z = reinterpret_cast<float4 *>(dq_acc + gr * D);
+        for (int e = lane; e < D / 4; e += 32)
+            z[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+
+// dQ = scale * dq_acc, rounded to bf16.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_dq_kernel(const float *__restrict__ dq_acc, __nv_bfloat16 *__restrict__ dq,
+                                                     int BH, int Tq, int Tq_pad, float scale)
+{
+    const size_t n8 = (size_t)BH * Tq * (D / 8);
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
+        const size_t row = i / (D / 8);
+        const int c8 = (int)(i - row * (D / 8));
+        const size_t bh = row / Tq;
+        const int r = (int)(row - bh * Tq);
+        const float4 *src = reinterpret_cast<const float4 *>(dq_acc + (bh * Tq_pad + r) * D + c8 * 8);
+        const float4 x0 = src[0], x1 = src[1];
+        uint4 w;
+        w.x = pack_bf16x2(x0.x * scale, x0.y * scale);
+        w.y = pack_bf16x2(x0.z * scale, x0.w * scale);
+        w.z = pack_bf16x2(x1.x * scale, x1.y * scale);
+        w.w = pack_bf16x2(x1.z * scale, x1.w * scale);
+        reinterpret_cast<uint4 *>(dq)[i] = w;
+    }
+}
+
+template <int D>
+int launch_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dO,
+               void *dq, void *dk, void *dv, int BH, int Tq, int Tk, int causal, float scale,
+               const BwdWorkspace &ws, int stages, cudaStream_t s)
+{
+    using L = BwdLayout<D>;
+    const int Tq_pad = (int)bwd_row_stride(Tq);
+    const int sms = device_sm_count();
+    // 1. preprocess
+    if ((stages & 1) && Tq > 0) {
+        const size_t rows = (size_t)BH * Tq_pad;
+        const size_t blocks = (rows + 7) / 8;
+        const int grid = (int)(blocks < (size_t)sms * 16 ? blocks : (size_t)sms * 16);
+        bwd_pre_kernel<D><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(o),
+                                               static_cast<const __nv_bfloat16 *>(dO), lse, ws.lse2, ws.delta,
+                                               ws.dq_acc, BH, Tq, Tq_pad);
+        if (cudaGetLastError() != cudaSuccess)
+            return ERR_CUDA;
+    }
+    // 2. tile loop
+    if ((stages & 2) && Tk > 0) {
+        CUtensorMap tq, tk, tv, tdo;
+        const int tq_rows = Tq > 0 ? Tq : 1;
+        int st = encode_tmap_3d(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, Tk, BH, 64, BK);
+        if (st == OK)
+            st = encode_tmap_3d(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, Tk, BH, 64, BK);
+        if (st == OK)
+            st = encode_tmap_3d(&tq, Tq > 0 ? q : k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, tq_rows, BH, 64, L::BQ);
+        if (st == OK)
+            st = encode_tmap_3d(&tdo, Tq > 0 ? dO : k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, tq_rows, BH, 64,
+                                L::BQ);
+        if (st != OK)
+            return st;
+        BwdArgs a;
+        a.lse2 = ws.lse2;
+        a.delta = ws.delta;
+        a.dq_acc = ws.dq_acc;
+        a.dk = static_cast<__nv_bfloat16 *>(dk);
+        a.dv = static_cast<__nv_bfloat16 *>(dv);
+        a.BH = BH;
+        a.Tq = Tq;
+        a.Tk = Tk;
+        a.Tq_pad = Tq_pad;
+        a.causal = causal;
+        a.scale = scale;
+        a.scale_log2 = scale * 1.4426950408889634f;
+        a.nkb = (Tk + BK - 1) / BK;
+        a.units = BH * a.nkb;
+        const double bytes_head = 2.0 * (Tq + Tk) * D * 2.0;   // Q, dO, K, V of one head
+        int gsz = (int)(48.0 * 1024 * 1024 / (bytes_head > 1 ? bytes_head : 1));
+        a.group = gsz < 1 ? 1 : (gsz > BH ? BH : gsz);
+        a.timeout_ns = wait_timeout_ns();
+        if (cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES) !=
+            cudaSuccess)
+            return ERR_CUDA;
+        const int grid = a.units < sms ? a.units : sms;
+        bwd_main_kernel<D><<<grid, L::NTHREADS, L::SMEM_BYTES, s>>>(tq, tk, tv, tdo, a);
+        if (cudaGetLastError() != cudaSuccess)
+            return ERR_CUDA;
+    }
+    // 3. dQ
+    if ((stages & 4) && Tq > 0) {
+        const size_t n8 = (size_t)BH * Tq * (D / 8);
+        const size_t blocks = (n8 + 255) / 256;
+        const int grid = (int)(blocks < (size_t)sms * 8 ? blocks : (size_t)sms * 8);
+        bwd_dq_kernel<D><<<grid, 256, 0, s>>>(ws.dq_acc, static_cast<__nv_bfloat16 *>(dq), BH, Tq, Tq_pad, scale);
+        if (cudaGetLastError() != cudaSuccess)
+            return ERR_CUDA;
+    }
+    return OK;
+}
+
+}  // namespace
+
+int bwd_launch(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dO, void *dq,
+               void *dk, void *dv, int BH, int Tq, int Tk, int d, int causal, float scale, const BwdWorkspace &ws,
+               int stages, cudaStream_t s)
+{
+    switch (d) {
+    case 64:
+        return launch_bwd<64>(q, k, v, o, lse, dO, dq, dk, dv, BH, Tq, Tk, causal, scale, ws, stages, s);
+    case 128:
+        return launch_bwd<128>(q, k, v, o, lse, dO, dq, dk, dv, BH, Tq, Tk, causal, scale, ws, stages, s);
+    default:
+        return ERR_UNSUPPORTED;
+    }
 }
 
 int bwd_status_fetch_clear(cudaStream_t s, int *host_word)
 {
     int zero = 0;
-    if (cudaMemcpyFromSymbolAsync(host_word, g_bwd_status, sizeof(int), 0, cudaMemcpyDeviceToHost, s) !=
-            cudaSuccess ||
+    if (cudaMemcpyFromSymbolAsync(host_word, g_bwd_status, sizeof(int), 0, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
         cudaMemcpyToSymbolAsync(g_bwd_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess)
         return ERR_CUDA;

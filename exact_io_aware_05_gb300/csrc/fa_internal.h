@@ -38,9 +38,11 @@ struct BwdWorkspace {
 size_t bwd_row_stride(int Tq);
 size_t bwd_workspace_bytes(int BH, int Tq, int d);
 BwdWorkspace bwd_workspace_carve(void *ws, int BH, int Tq, int d);
+// stages: bit 0 = preprocess (D, lse2, zero dQ accumulator), bit 1 = tile loop
+// (dK, dV, dQ accumulation), bit 2 = dQ scale-and-round.
 int bwd_launch(const void *q, const void *k, const void *v, const void *o, const float *lse,
                const void *dO, void *dq, void *dk, void *dv, int BH, int Tq, int Tk, int d,
-               int causal, float scale, const BwdWorkspace &ws, cudaStream_t s);
+               int causal, float scale, const BwdWorkspace &ws, int stages, cudaStream_t s);
 
 // Device status words of the kernel translation units: read, add into *acc
 // the first nonzero value, and clear.  Stream-ordered; the caller syncs.

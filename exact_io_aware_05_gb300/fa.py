@@ -30,6 +30,8 @@ _lib.fa_bwd_workspace_bytes.argtypes = [_i, _i, _i, _i, _i]
 _lib.fa_bwd_workspace_bytes.restype = _sz
 _lib.fa_bwd.argtypes = [_vp] * 9 + [_i] * 6 + [_f, _vp, _sz, _vp]
 _lib.fa_bwd.restype = _i
+_lib.fa_bwd_stage.argtypes = [_i] + [_vp] * 9 + [_i] * 6 + [_f, _vp, _sz, _vp]
+_lib.fa_bwd_stage.restype = _i
 _lib.fa_sync_status.argtypes = [_vp]
 _lib.fa_sync_status.restype = _i
 _lib.fa_status_string.argtypes = [_i]
@@ -128,6 +130,17 @@ def fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, causal: bool, scale: float, workspac
     _check("fa_bwd", _lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
                                  _ptr(dk), _ptr(dv), B, H, Tq, Tk, d, int(bool(causal)), float(scale),
                                  _ptr(workspace), nbytes, _stream(stream)))
+
+
+def fa_bwd_stage(stage: int, q, k, v, o, lse, dO, dq, dk, dv, causal: bool, scale: float,
+                 workspace: torch.Tensor, stream=None) -> None:
+    """Stage 1, 2 or 3 of fa_bwd (preprocess, tile loop, dQ finish); same arguments."""
+    B, H, Tq, Tk, d = _shapes(q, k)
+    nbytes = workspace.numel() * workspace.element_size()
+    _check("fa_bwd_stage", _lib.fa_bwd_stage(int(stage), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                             _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv), B, H, Tq, Tk, d,
+                                             int(bool(causal)), float(scale), _ptr(workspace), nbytes,
+                                             _stream(stream)))
 
 
 def fa_sync_status(stream=None) -> int:

@@ -98,6 +98,21 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
            void *workspace, size_t workspace_bytes, fa_stream_t stream);
 
 /*
+ * One stage of fa_bwd, for callers that schedule or time the three kernels
+ * separately: stage 1 computes D_r = dO_r . O_r and the log2-domain lse into
+ * the workspace and zeroes the dQ accumulator; stage 2 runs the tile loop
+ * (recomputes P from lse, writes dK and dV, adds dQ into the accumulator);
+ * stage 3 scales the accumulator by `scale` and writes dq.  Running stages
+ * 1, 2, 3 in that order on one stream with the same arguments and workspace
+ * is exactly fa_bwd.  Arguments, validation and errors are those of fa_bwd;
+ * stage outside 1..3 returns FA_ERR_INVALID_ARG.
+ */
+int fa_bwd_stage(int stage, const void *q, const void *k, const void *v, const void *o,
+                 const float *lse, const void *dO, void *dq, void *dk, void *dv,
+                 int B, int H, int Tq, int Tk, int d, int causal, float scale,
+                 void *workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/*
  * Synchronises `stream`, then returns and clears the device status word of
  * the current device: FA_OK, FA_ERR_TIMEOUT (a kernel's bounded wait ran out;
  * its outputs are invalid) or FA_ERR_CUDA (the synchronise failed).
