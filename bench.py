@@ -60,6 +60,31 @@ def measured_peaks() -> dict:
         return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
 
 
+PROFILE_OF = {"bwd_main": ("profiles/bwd_main_d128_b2h32_t4096_causal.md", ("fa_bwd_sm103.cu", "fa_common.cuh")),
+              "fwd": ("profiles/fwd_kernel_d128_b2h32_t4096_causal.md", ("fa_fwd_sm103.cu", "fa_common.cuh"))}
+
+
+def ncu_traffic(kernel: str) -> int | None:
+    """DRAM bytes (read + write) per full-size launch from the committed ncu summary of
+    `kernel`, or None when the kernel's sources changed since that capture."""
+    import hashlib
+    import re
+    path, srcs = PROFILE_OF[kernel]
+    try:
+        text = open(os.path.join(ROOT, path)).read()
+        h = hashlib.sha256()
+        for f in srcs:
+            h.update(open(os.path.join(ROOT, "exact_io_aware_05_gb300", "csrc", f), "rb").read())
+        sha = re.search(r"source-sha256-16:\s*([0-9a-f]{16})", text).group(1)
+        if sha != h.hexdigest()[:16]:
+            return None
+        if WORKLOAD["B"] != 8:
+            return None
+        return int(re.search(r"dram-bytes-per-launch-b8h32:\s*(\d+)", text).group(1))
+    except Exception:
+        return None
+
+
 def dist_info():
     return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
             int(os.environ.get("WORLD_SIZE", "1")))
@@ -346,7 +371,7 @@ def run_ours(args) -> None:
                    "bwd": {"ms": pre_ms + main_ms + dq_ms, "tflops": bwd_tf, "pct_of_peak": 100 * bwd_tf / peak,
                            "preprocess_ms": pre_ms, "tile_loop_ms": main_ms, "dq_finish_ms": dq_ms}},
         "roofline": {"kernel": dom[0], "bound": "tensor", "achieved": dom[1], "peak": peak, "unit": "TFLOP/s",
-                     "frac": dom[1] / peak, "traffic": None,
+                     "frac": dom[1] / peak, "traffic": ncu_traffic(dom[0]),
                      "peak_source": f"{peaks['source']} bf16 (burst), MEASURED_PEAKS.json"},
         "gpu_launches": KERNELS_PER_STEP * args.steps,
         "e2e": e2e,
@@ -365,7 +390,12 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=WORKLOAD["B"],
+                    help="batch size (default 8, the benchmark workload; smaller only for profiling)")
     args = ap.parse_args()
+    if args.batch != WORKLOAD["B"]:
+        WORKLOAD["B"] = args.batch
+        WORKLOAD["name"] = f"attention fwd+bwd B{args.batch} H32 N4096 d128 causal (profiling size)"
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
