@@ -32,6 +32,8 @@ _lib.fa_bwd.argtypes = [_vp] * 9 + [_i] * 6 + [_f, _vp, _sz, _vp]
 _lib.fa_bwd.restype = _i
 _lib.fa_bwd_stage.argtypes = [_i] + [_vp] * 9 + [_i] * 6 + [_f, _vp, _sz, _vp]
 _lib.fa_bwd_stage.restype = _i
+_lib.fa_bwd_noalloc.argtypes = [_vp] * 9 + [_i] * 6 + [_f, _vp]
+_lib.fa_bwd_noalloc.restype = _i
 _lib.fa_sync_status.argtypes = [_vp]
 _lib.fa_sync_status.restype = _i
 _lib.fa_status_string.argtypes = [_i]
@@ -141,6 +143,16 @@ def fa_bwd_stage(stage: int, q, k, v, o, lse, dO, dq, dk, dv, causal: bool, scal
                                              _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv), B, H, Tq, Tk, d,
                                              int(bool(causal)), float(scale), _ptr(workspace), nbytes,
                                              _stream(stream)))
+
+
+def fa_bwd_noalloc(q, k, v, o, lse, dO, dq, dk, dv, causal: bool, scale: float, stream=None) -> None:
+    """fa_bwd without a workspace argument, for callers that cannot allocate device memory:
+    the scratch is a fixed array inside the library (see include/fa.h for its size limit
+    and for why overlapping calls on one device must not be issued)."""
+    B, H, Tq, Tk, d = _shapes(q, k)
+    _check("fa_bwd_noalloc", _lib.fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO),
+                                                 _ptr(dq), _ptr(dk), _ptr(dv), B, H, Tq, Tk, d,
+                                                 int(bool(causal)), float(scale), _stream(stream)))
 
 
 def fa_sync_status(stream=None) -> int:

@@ -113,6 +113,40 @@ int fa_bwd_stage(int stage, const void *q, const void *k, const void *v, const v
                  void *workspace, size_t workspace_bytes, fa_stream_t stream);
 
 /*
+ * Size of the fixed device scratch array behind fa_bwd_noalloc (64 MiB).  It
+ * holds fa_bwd_workspace_bytes(B, H, Tq, Tk, d) bytes when, for example,
+ * B*H*Tq_pad <= 126,000 rows at d = 128 (B8 H8 T2048, B1 H32 T3840).
+ */
+#define FA_BWD_NOALLOC_SCRATCH_BYTES (64u << 20)
+
+/*
+ * fa_bwd for callers that cannot allocate device memory.  The pages have no
+ * counterpart: this serves callers that are handed only their input and
+ * output buffers and may not call cudaMalloc -- plug-ins whose host framework
+ * owns all device memory and offers them no allocator, or latency-critical
+ * code that cannot take cudaMalloc's implicit device synchronisation.
+ * Arguments, results and errors are those of fa_bwd without the workspace:
+ * the scratch comes from a fixed array of FA_BWD_NOALLOC_SCRATCH_BYTES that
+ * the library keeps in device memory (each device holds it until the process
+ * exits).  The call allocates nothing.
+ *   - Sizes whose fa_bwd_workspace_bytes(...) exceeds
+ *     FA_BWD_NOALLOC_SCRATCH_BYTES return FA_ERR_UNSUPPORTED before any CUDA
+ *     call; use fa_bwd with a caller-owned workspace for those.
+ *   - The first call on a device looks the array's device address up
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - Every call on a device shares the one array.  Each call rewrites all of
+ *     the scratch it uses before reading it (the dQ accumulator is zeroed),
+ *     so nothing carries over between calls, but calls that overlap on the
+ *     GPU (different streams or threads on one device) race and corrupt each
+ *     other's results: order them, e.g. on one stream.
+ */
+int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                   const void *dO, void *dq, void *dk, void *dv,
+                   int B, int H, int Tq, int Tk, int d, int causal, float scale,
+                   fa_stream_t stream);
+
+/*
  * Synchronises `stream`, then returns and clears the device status word of
  * the current device: FA_OK, FA_ERR_TIMEOUT (a kernel's bounded wait ran out;
  * its outputs are invalid) or FA_ERR_CUDA (the synchronise failed).
