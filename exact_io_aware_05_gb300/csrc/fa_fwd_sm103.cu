@@ -71,7 +71,7 @@ struct FwdLayout {
     static constexpr int B_FULL = 0, B_EMPTY = NSLOT, B_QFULL = 2 * NSLOT, B_QEMPTY = 2 * NSLOT + 1,
                          B_SFULL = 2 * NSLOT + 2, B_PFULL = 2 * NSLOT + 4, B_ODONE = 2 * NSLOT + 6,
                          B_OEMPTY = 2 * NSLOT + 8, B_DRAIN = 2 * NSLOT + 10, B_PREAD = 2 * NSLOT + 11,
-                         B_OFINAL = 2 * NSLOT + 13, NBAR = 2 * NSLOT + 15;
+                         B_OFINAL = 2 * NSLOT + 13, B_DRAIN1 = 2 * NSLOT + 15, NBAR = 2 * NSLOT + 16;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;   // tmem base (u32), abort flag (int)
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1024-byte alignment
     static constexpr int S_COL = 0;                  // S buffer b at columns [b*BC, (b+1)*BC)
@@ -204,12 +204,13 @@ __global__ void __launch_bounds__(FwdLayout<D>::NTHREADS, 1)
     const uint32_t warp = warp_id(), lane = lane_id();
 
     if (threadIdx.x == 0) {
+        // with two query tiles, each tile's MMA warp releases every K/V slot and the Q tiles
         for (int s = 0; s < NSLOT; ++s) {
             mbar_init(bar(L::B_FULL + s), 1);
-            mbar_init(bar(L::B_EMPTY + s), 1);
+            mbar_init(bar(L::B_EMPTY + s), NQ);
         }
         mbar_init(bar(L::B_QFULL), 1);
-        mbar_init(bar(L::B_QEMPTY), 1);
+        mbar_init(bar(L::B_QEMPTY), NQ);
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(L::B_SFULL + b), 1);
             mbar_init(bar(L::B_PFULL + b), 128);
@@ -221,6 +222,7 @@ __global__ void __launch_bounds__(FwdLayout<D>::NTHREADS, 1)
         mbar_init(bar(L::B_OFINAL), 1);
         mbar_init(bar(L::B_OFINAL + 1), 1);
         mbar_init(bar(L::B_DRAIN), 1);
+        mbar_init(bar(L::B_DRAIN1), 1);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tm_q);
@@ -273,20 +275,28 @@ __global__ void __launch_bounds__(FwdLayout<D>::NTHREADS, 1)
                     ++n_loads;
                     return true;
                 };
-                const bool ok = walk_ops(
-                    p.J,
-                    [&](int k) {
-                        int t, j;
-                        bool first, last;
-                        job_of<NQ>(p, k, t, j, first, last);
-                        return first ? load(&tm_k, j) : true;
-                    },
-                    [&](int k) {
-                        int t, j;
-                        bool first, last;
-                        job_of<NQ>(p, k, t, j, first, last);
-                        return first ? load(&tm_v, j) : true;
-                    });
+                bool ok = true;
+                if constexpr (NQ == 2) {
+                    // each tile's MMA warp consumes K_0, V_0, K_1, V_1, ... in this order
+                    const int nmax = max(p.n[0], p.n[1]);
+                    for (int j = 0; j < nmax && ok; ++j)
+                        ok = load(&tm_k, j) && load(&tm_v, j);
+                } else {
+                    ok = walk_ops(
+                        p.J,
+                        [&](int k) {
+                            int t, j;
+                            bool first, last;
+                            job_of<NQ>(p, k, t, j, first, last);
+                            return first ? load(&tm_k, j) : true;
+                        },
+                        [&](int k) {
+                            int t, j;
+                            bool first, last;
+                            job_of<NQ>(p, k, t, j, first, last);
+                            return first ? load(&tm_v, j) : true;
+                        });
+                }
                 if (!ok)
                     break;
             }
@@ -298,8 +308,99 @@ __global__ void __launch_bounds__(FwdLayout<D>::NTHREADS, 1)
                 mbar_wait_drain(bar(L::B_QFULL), (n_q - 1) & 1, a.timeout_ns);
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
+    } else if (NQ == 2 && (warp == 1 || warp == 2)) {
+        // ------------------------------------------------ MMA issuer of query tile t
+        // One issuing thread per tile: a single thread cannot issue tcgen05.mma fast enough
+        // to keep the tensor core busy with N = 128 products, two interleave.
+        if (lane == 0) {
+            const int t = (int)warp - 1;
+            const uint32_t s_col = L::S_COL + t * BC, o_col = L::O_COL + t * D;
+            const uint32_t qa = sbase + L::OFF_Q + t * L::Q_TILE;
+            const uint32_t drain_bar = bar(t == 0 ? L::B_DRAIN : L::B_DRAIN1);
+            uint32_t ld = 0, q_seen = 0, pvn = 0, epi = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+                const Plan p = make_plan<D>(u, a);
+                if (p.J == 0)
+                    continue;
+                if (!mbar_wait(bar(L::B_QFULL), q_seen & 1, ctx, SITE_M_QFULL))
+                    break;
+                ++q_seen;
+                const int nt = p.n[t], nmax = max(p.n[0], p.n[1]);
+                if (nt == 0)
+                    mbar_arrive(bar(L::B_QEMPTY));      // this tile reads no Q in this unit
+                for (int j = 0; j < nmax; ++j) {
+                    // K_j: S_t = Q_t K_j^T
+                    const uint32_t ks = ld % NSLOT;
+                    if (!mbar_wait(bar(L::B_FULL + ks), (ld / NSLOT) & 1, ctx, SITE_M_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                    ++ld;
+                    if (j < nt) {
+                        // S_t overwrites the columns from which the previous PV of this tile
+                        // read P: that PV must have completed
+                        if (pvn > 0 && !mbar_wait(bar(L::B_ODONE + t), (pvn - 1) & 1, ctx, SITE_M_PREAD)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t ka = sbase + L::OFF_SLOT + ks * L::KV_TILE;
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = (kk & 3) * 32;
+                            mma_ss(tmem + s_col, sdesc_sw128(qa + (kk >> 2) * L::Q_CHUNK + off, 16, 1024),
+                                   sdesc_sw128(ka + (kk >> 2) * L::KV_CHUNK + off, 16, 1024), L::IDESC_S,
+                                   kk > 0 ? 1u : 0u);
+                        }
+                        tc_commit(bar(L::B_SFULL + t));
+                        tc_commit(bar(L::B_EMPTY + ks));
+                        if (j == nt - 1)
+                            tc_commit(bar(L::B_QEMPTY));
+                    } else {
+                        mbar_arrive(bar(L::B_EMPTY + ks));  // K_j is only for the other tile
+                    }
+                    // V_j: O_t += P_t V_j
+                    const uint32_t vs = ld % NSLOT;
+                    if (!mbar_wait(bar(L::B_FULL + vs), (ld / NSLOT) & 1, ctx, SITE_M_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                    ++ld;
+                    if (j < nt) {
+                        if (!mbar_wait(bar(L::B_PFULL + t), pvn & 1, ctx, SITE_M_PFULL)) {
+                            ok = false;
+                            break;
+                        }
+                        if (j == 0 && epi > 0 &&
+                            !mbar_wait(bar(L::B_OEMPTY + t), (epi - 1) & 1, ctx, SITE_M_OEMPTY)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t va = sbase + L::OFF_SLOT + vs * L::KV_TILE;
+#pragma unroll
+                        for (int kk = 0; kk < BC / 16; ++kk)
+                            mma_ts(tmem + o_col, tmem + s_col + kk * 8, sdesc_sw128(va + kk * 16 * 128, L::KV_CHUNK, 1024),
+                                   L::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+                        tc_commit(bar(L::B_ODONE + t));   // O~ current and P read: one signal
+                        tc_commit(bar(L::B_EMPTY + vs));
+                        ++pvn;
+                        if (j == nt - 1) {
+                            tc_commit(bar(L::B_OFINAL + t));
+                            ++epi;
+                        }
+                    } else {
+                        mbar_arrive(bar(L::B_EMPTY + vs));
+                    }
+                }
+            }
+            tc_commit(drain_bar);
+            mbar_wait_drain(drain_bar, 0, a.timeout_ns);
+        }
+        __syncwarp();
+    } else if (NQ == 1 && warp == 1) {
+        // ------------------------------------------------ MMA issuer (one query tile)
         if (lane == 0) {
             uint32_t ld = 0, kg = 0, q_seen = 0;
             uint32_t epi[2] = {0, 0};
@@ -394,16 +495,14 @@ __global__ void __launch_bounds__(FwdLayout<D>::NTHREADS, 1)
         const int rit = (int)(quarter * 32 + lane);    // row within the tile
         const float sl2 = a.scale_log2;
         const uint32_t lane_base = tmem + ((quarter * 32u) << 16);
-        uint32_t kg = 0, pv = 0, ep = 0;
+        uint32_t pv = 0, ep = 0;   // jobs and epilogues of this tile so far
         for (int u = blockIdx.x; u < a.units; u += gridDim.x) {
             const Plan p = make_plan<D>(u, a);
             const int r = p.row0 + t * BR + rit;
             const bool row_ok = r < a.Tq;
             const size_t grow = (size_t)p.bh * a.Tq + r;
-            if (!p.rows[t]) {
-                kg += p.J;
+            if (!p.rows[t])
                 continue;
-            }
             if (p.n[t] == 0) {   // no key is allowed for any row of this tile
                 if (row_ok) {
                     uint4 *dst = reinterpret_cast<uint4 *>(a.o + grow * D);
@@ -411,32 +510,34 @@ __global__ void __launch_bounds__(FwdLayout<D>::NTHREADS, 1)
                         dst[i] = make_uint4(0, 0, 0, 0);
                     a.lse[grow] = -INFINITY;
                 }
-                kg += p.J;
                 continue;
             }
             float m = -INFINITY, l = 0.f;
             bool ok = true;
-            for (int k = 0; k < p.J && ok; ++k) {
-                int tt, j;
-                bool first, last;
-                job_of<NQ>(p, k, tt, j, first, last);
-                if (tt != t)
-                    continue;
-                const uint32_t b = (kg + k) & 1;
-                if (!mbar_wait(bar(L::B_SFULL + b), ((kg + k) >> 1) & 1, ctx, SITE_S_SFULL)) {
+            for (int j = 0; j < p.n[t] && ok; ++j) {
+                // two tiles: S buffer t, one phase per job of this tile; one tile: the two
+                // S buffers alternate between consecutive jobs
+                const uint32_t b = NQ == 2 ? (uint32_t)t : (pv & 1);
+                const uint32_t ph = NQ == 2 ? (pv & 1) : ((pv >> 1) & 1);
+                if (!mbar_wait(bar(L::B_SFULL + b), ph, ctx, SITE_S_SFULL)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
+                // S row: all column chunks in flight, one wait
+                uint32_t sv[BC / 32][32];
+#pragma unroll
+                for (int c = 0; c < BC / 32; ++c)
+                    tmem_ld_x32_nowait(lane_base + L::S_COL + b * BC + c * 32, sv[c]);
+#pragma unroll
+                for (int c = 0; c < BC / 32; ++c)
+                    tmem_wait_ld_x32(sv[c]);
                 float s[BC];
 #pragma unroll
-                for (int c = 0; c < BC / 32; ++c) {
-                    uint32_t v[32];
-                    tmem_ld_x32(lane_base + L::S_COL + b * BC + c * 32, v);
+                for (int c = 0; c < BC / 32; ++c)
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
-                        s[c * 32 + i] = __uint_as_float(v[i]);
-                }
+                        s[c * 32 + i] = __uint_as_float(sv[c][i]);
                 // mask: tail keys beyond Tk, and keys after the causal limit
                 const int kv0 = j * BC;
                 const int first_row = p.row0 + t * BR;
@@ -452,15 +553,17 @@ __global__ void __launch_bounds__(FwdLayout<D>::NTHREADS, 1)
                         if (i >= cl)
                             s[i] = -INFINITY;
                 }
-                float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+                // row max: four independent chains of three-input max
+                float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+                static_assert(BC % 8 == 0, "row max covers BC in steps of 8");
 #pragma unroll
-                for (int i = 4; i < BC; i += 4) {
-                    mx0 = fmaxf(mx0, s[i]);
-                    mx1 = fmaxf(mx1, s[i + 1]);
-                    mx2 = fmaxf(mx2, s[i + 2]);
-                    mx3 = fmaxf(mx3, s[i + 3]);
+                for (int i = 0; i < BC; i += 8) {
+                    mx0 = fmax3(mx0, s[i], s[i + 1]);
+                    mx1 = fmax3(mx1, s[i + 2], s[i + 3]);
+                    mx2 = fmax3(mx2, s[i + 4], s[i + 5]);
+                    mx3 = fmax3(mx3, s[i + 6], s[i + 7]);
                 }
-                const float m_new = fmaxf(m, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)));
+                const float m_new = fmaxf(m, fmax3(mx0, mx1, fmax3(mx2, mx3, -INFINITY)));
                 const bool resc = (m != -INFINITY) && (m_new > m);
                 float alpha = 1.f;
                 if (m == -INFINITY) {
@@ -473,20 +576,29 @@ __global__ void __launch_bounds__(FwdLayout<D>::NTHREADS, 1)
                 // P~ = exp2(c log2e (s - m)), packed to bf16 pairs over the first BC/2
                 // columns of this S buffer, 32 keys at a time
                 const float mref = (m == -INFINITY) ? 0.f : m * sl2;
-                float l0 = 0.f, l1 = 0.f;
+                float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
 #pragma unroll
                 for (int c = 0; c < BC / 32; ++c) {
                     uint32_t pk[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float p0 = ex2_approx(fmaf(s[c * 32 + 2 * i], sl2, -mref));
-                        const float p1 = ex2_approx(fmaf(s[c * 32 + 2 * i + 1], sl2, -mref));
-                        l0 += p0;
-                        l1 += p1;
-                        pk[i] = pack_bf16x2(p0, p1);
+                    for (int i = 0; i < 16; i += 2) {
+                        const int e = c * 32 + 2 * i;
+                        float x0, x1, x2, x3;
+                        ffma2(x0, x1, s[e], s[e + 1], sl2, sl2, -mref, -mref);
+                        ffma2(x2, x3, s[e + 2], s[e + 3], sl2, sl2, -mref, -mref);
+                        x0 = ex2_approx(x0);
+                        x1 = ex2_approx(x1);
+                        x2 = ex2_approx(x2);
+                        x3 = ex2_approx(x3);
+                        fadd2(l0, l1, l0, l1, x0, x1);
+                        fadd2(l2, l3, l2, l3, x2, x3);
+                        pk[i] = pack_bf16x2(x0, x1);
+                        pk[i + 1] = pack_bf16x2(x2, x3);
                     }
                     tmem_st_x16(lane_base + L::S_COL + b * BC + c * 16, pk);
                 }
+                l0 += l2;
+                l1 += l3;
                 l += l0 + l1;
                 if (__any_sync(0xffffffffu, resc)) {
                     // O~ must hold the previous PV of this tile before it is rescaled
@@ -501,8 +613,12 @@ __global__ void __launch_bounds__(FwdLayout<D>::NTHREADS, 1)
                         const uint32_t ta = lane_base + L::O_COL + t * D + c * 32;
                         tmem_ld_x32(ta, v);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+                        for (int i = 0; i < 32; i += 2) {
+                            float y0, y1;
+                            fmul2(y0, y1, __uint_as_float(v[i]), __uint_as_float(v[i + 1]), alpha, alpha);
+                            v[i] = __float_as_uint(y0);
+                            v[i + 1] = __float_as_uint(y1);
+                        }
                         tmem_st_x32(ta, v);
                     }
                 }
@@ -540,7 +656,6 @@ __global__ void __launch_bounds__(FwdLayout<D>::NTHREADS, 1)
                 a.lse[grow] = l > 0.f ? (m * sl2 + log2f(l)) * 0.69314718055994530942f : -INFINITY;
             tc_fence_before();
             mbar_arrive(bar(L::B_OEMPTY + t));
-            kg += p.J;
         }
     }
     // ---------------------------------------------------- teardown
