@@ -13,24 +13,25 @@
 // recomputation").
 //
 // GB300 design:
-//   * three kernels on one stream: bwd_pre (D, log2-domain lse, dQ accumulator
-//     zeroed), bwd_main (the tile loop below), bwd_dq (scale and round dQ);
+//   * three kernels on one stream: bwd_pre (-D, -lse in log2 units, dQ
+//     accumulator zeroed), bwd_main (the tile loop below), bwd_dq (scale and
+//     round dQ);
 //   * bwd_main is persistent; a unit is one 128-key block of one head, taken
-//     longest-first within groups of heads;
-//   * warp 0 streams K_j, V_j once per unit and Q_i, dO_i, lse_i, D_i per query
-//     block through a 3-stage ring (TMA tiles + bulk copies); warp 1 issues all
-//     tcgen05.mma; two softmax warpgroups each rebuild half of a tile's
-//     P^T and dS^T from S^T and dP^T in tensor memory; a fourth warpgroup
-//     drains dQ from tensor memory into the fp32 accumulator with atomic adds
-//     and writes dK, dV at the end of the unit;
-//   * tensor memory: S^T and dP^T (128 keys x BQ queries), two dQ buffers, and
-//     the dV, dK accumulators.  For d = 128 the query block is 64 rows and dQ
-//     is formed transposed (dQ^T = K_j^T dS^T, M = d) so that every region fits
-//     in 512 columns; for d = 64 the query block is 128 rows and dQ = dS K_j;
-//   * the dQ product of block g is issued after the S/dP products of block
-//     g+1, so the tensor core works while the softmax warpgroups run;
-//   * every MMA that overwrites a tensor-memory region waits for the MMA that
-//     last read it as an operand, and every wait is bounded.
+//     longest-first within groups of heads; query blocks are 128 rows, so every
+//     product is a full M128 x N128 (d = 128) tensor-core instruction;
+//   * warp 0 streams K_j, V_j once per unit and Q_i, dO_i per query block
+//     through a ring of stages (TMA); warp 1 issues all tcgen05.mma; two
+//     softmax warpgroups each rebuild half of a block's P^T and dS^T from S^T
+//     and dP^T in tensor memory (lse and D come from L1-cached global loads);
+//     a fourth warpgroup drains dQ from tensor memory into the fp32
+//     accumulator with atomic adds and writes dK, dV at the end of the unit;
+//   * tensor memory (512 columns): S^T, dP^T (128 keys x 128 queries) and the
+//     dV, dK accumulators.  For d = 128 dQ is formed transposed
+//     (dQ^T = K_j^T dS^T, M = d) in the S^T columns once dV has read P^T
+//     from them; for d = 64, dQ = dS K_j has two buffers of its own and is
+//     issued one block late, under the next block's softmax;
+//   * every MMA that overwrites a tensor-memory region waits for the MMA (or
+//     the drain) that last read it, and every wait is bounded.
 #include "fa_common.cuh"
 #include "fa_internal.h"
 
@@ -41,68 +42,58 @@ __device__ int g_bwd_status;   // device status word of the backward kernels
 namespace {
 
 constexpr int BK = 128;   // keys per unit (= MMA M for S^T, dP^T, dV, dK)
-constexpr int NST = 3;    // Q/dO stages
-
-template <int D>
-struct BwdCfg;
-template <>
-struct BwdCfg<64> {
-    static constexpr int BQ = 128;       // queries per block
-    static constexpr bool DQT = false;   // dQ = dS K_j (M = queries)
-};
-template <>
-struct BwdCfg<128> {
-    static constexpr int BQ = 64;
-    static constexpr bool DQT = true;    // dQ^T = K_j^T dS^T (M = d)
-};
+constexpr int BQ = 128;   // queries per block (= N of S^T, dP^T; K of dV, dK)
 
 template <int D>
 struct BwdLayout {
-    static constexpr int BQ = BwdCfg<D>::BQ;
-    static constexpr bool DQT = BwdCfg<D>::DQT;
+    // d = 128: dQ^T = K_j^T dS^T (M = d) takes the dP^T columns of tensor memory once the
+    // softmax has read dP^T, so that S^T, dP^T, dV and dK (4 x 128 columns) fit;
+    // d = 64: dQ = dS K_j has two buffers of its own.
+    static constexpr bool DQ_ALIAS = (D == 128);
     static constexpr int KCH = D / 64;
     static constexpr int KV_CHUNK = BK * 128;            // one 64-column chunk of K_j or V_j
     static constexpr int KV_TILE = KCH * KV_CHUNK;
     static constexpr int Q_CHUNK = BQ * 128;
     static constexpr int Q_TILE = KCH * Q_CHUNK;
+    static constexpr int NST = D == 128 ? 2 : 3;          // Q/dO stages
+    static constexpr int ST_Q = 0, ST_DO = Q_TILE, ST_BYTES = 2 * Q_TILE;
     static constexpr int DS_CHUNK = BK * 128;            // dS^T: 128 keys x 64 queries bf16
     static constexpr int DS_TILE = (BQ / 64) * DS_CHUNK;
-    // stage: Q_i, dO_i, lse2_i, D_i
-    static constexpr int ST_Q = 0, ST_DO = Q_TILE, ST_LSE = 2 * Q_TILE, ST_D = 2 * Q_TILE + BQ * 4;
-    static constexpr int ST_BYTES = ((2 * Q_TILE + 2 * BQ * 4) + 1023) / 1024 * 1024;
+    static constexpr int NDS = DQ_ALIAS ? 1 : 2;         // dS^T buffers in shared memory
     static constexpr int OFF_K = 0, OFF_V = KV_TILE, OFF_ST = 2 * KV_TILE;
     static constexpr int OFF_DS = OFF_ST + NST * ST_BYTES;
-    static constexpr int OFF_BAR = OFF_DS + 2 * DS_TILE;
+    static constexpr int OFF_LSE = OFF_DS + NDS * DS_TILE;   // -lse log2(e) of the current block
+    static constexpr int OFF_DEL = OFF_LSE + BQ * 4;          // -D of the current block
+    static constexpr int OFF_BAR = OFF_DEL + BQ * 4;
     enum : int {
         B_KVFULL = 0, B_KVEMPTY, B_STFULL, B_STEMPTY = B_STFULL + NST, B_SFULL = B_STEMPTY + NST,
-        B_PFULL, B_DVDONE, B_DKDONE, B_DQFULL, B_DQEMPTY = B_DQFULL + 2, B_DKVFULL = B_DQEMPTY + 2,
-        B_DKVEMPTY, B_DRAIN, NBAR
+        B_DPFULL, B_PFULL, B_DSFULL, B_DVDONE, B_DQFULL, B_DQEMPTY = B_DQFULL + 2, B_DKVFULL = B_DQEMPTY + 2,
+        B_DKVEMPTY, B_LFULL, B_DFULL, B_DRAIN, NBAR
     };
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
     // tensor memory columns
-    static constexpr int T_S = 0, T_DP = BQ;
-    static constexpr int T_DQ = DQT ? 2 * BQ : 256 + 2 * D;     // two buffers of DQ_COLS
-    static constexpr int DQ_COLS = DQT ? BQ : D;
-    static constexpr int T_DV = DQT ? 2 * BQ + 2 * DQ_COLS : 256, T_DK = T_DV + D;
+    static constexpr int T_S = 0, T_DP = BQ, T_DV = 2 * BQ, T_DK = 2 * BQ + D;
+    static constexpr int T_DQ = DQ_ALIAS ? T_DP : T_DK + D;
+    static constexpr int DQ_COLS = DQ_ALIAS ? BQ : D;
     static constexpr int TMEM_COLS = 512;
-    static_assert(T_DK + D <= TMEM_COLS && T_DQ + 2 * DQ_COLS <= TMEM_COLS, "tensor memory budget");
+    static_assert(T_DK + D <= TMEM_COLS && T_DQ + (DQ_ALIAS ? 1 : 2) * DQ_COLS <= TMEM_COLS, "tensor memory budget");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
     static constexpr int NTHREADS = 512;
-    // instruction descriptors
     static constexpr uint32_t ID_SDP = idesc_bf16_f32(128, BQ, false, false);   // K_j Q_i^T, V_j dO_i^T
     static constexpr uint32_t ID_DKV = idesc_bf16_f32(128, D, false, true);     // P^T dO_i, dS^T Q_i
-    static constexpr uint32_t ID_DQ = DQT ? idesc_bf16_f32(128, BQ, true, true)   // K_j^T dS^T
-                                          : idesc_bf16_f32(128, D, true, true);   // dS K_j
+    static constexpr uint32_t ID_DQ = DQ_ALIAS ? idesc_bf16_f32(128, BQ, true, true)   // K_j^T dS^T
+                                               : idesc_bf16_f32(128, D, true, true);   // dS K_j
 };
 
 enum WaitSite : int {
-    SITE_P_KVEMPTY = 1, SITE_P_STEMPTY, SITE_M_KVFULL, SITE_M_STFULL, SITE_M_DVDONE, SITE_M_DKDONE,
-    SITE_M_PFULL, SITE_M_DKVEMPTY, SITE_M_DQEMPTY, SITE_S_SFULL, SITE_D_DQFULL, SITE_D_DKVFULL
+    SITE_P_KVEMPTY = 1, SITE_P_STEMPTY, SITE_M_KVFULL, SITE_M_STFULL, SITE_M_DVDONE, SITE_M_DSFULL,
+    SITE_M_DPDV, SITE_M_DQEMPTY, SITE_S_SFULL, SITE_S_DPFULL, SITE_D_DQFULL, SITE_D_DKVFULL, SITE_L_PFULL,
+    SITE_L_DSFULL, SITE_S_LFULL, SITE_S_DFULL
 };
 
 struct BwdArgs {
-    const float *lse2, *delta;
+    const float *nlse2, *ndelta;   // -lse * log2(e) and -D per (padded) query row
     float *dq_acc;
     __nv_bfloat16 *dk, *dv;
     int BH, Tq, Tk, Tq_pad, causal;
@@ -116,10 +107,8 @@ struct Unit {
     int i0, nq;    // first query block, number of query blocks
 };
 
-template <int D>
 __device__ __forceinline__ Unit make_unit(int u, const BwdArgs &a)
 {
-    using L = BwdLayout<D>;
     const int per_group = a.group * a.nkb;
     const int g = u / per_group;
     const int w = u - g * per_group;
@@ -128,17 +117,22 @@ __device__ __forceinline__ Unit make_unit(int u, const BwdArgs &a)
     Unit x;
     x.bh = g * a.group + (w - lvl * heads_here);
     x.j = lvl;
-    const int nqb = (a.Tq + L::BQ - 1) / L::BQ;
+    const int nqb = (a.Tq + BQ - 1) / BQ;
     int first_row = 0;
     if (a.causal) {
         const long r = (long)x.j * BK - (a.Tk - a.Tq);   // first query that sees key j*BK
         first_row = r < 0 ? 0 : (int)min(r, (long)a.Tq);
     }
-    x.i0 = first_row / L::BQ;
+    x.i0 = first_row / BQ;
     x.nq = nqb - x.i0;
     if (x.nq < 0)
         x.nq = 0;
     return x;
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
@@ -148,9 +142,36 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
                  : "memory");
 }
 
-__device__ __forceinline__ void fence_proxy_async_smem()
+// A-operand column (P^T, bf16 pairs) of K-step kk: each softmax warpgroup packs its 64
+// query columns at the start of its own 64-column half of the S^T region.
+__device__ __forceinline__ uint32_t half_packed_col(int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; }
+
+// P = exp2(c log2(e) S - lse log2(e)) for 32 query columns of one key row, in place.
+template <bool MASK>
+__device__ __forceinline__ void softmax_p32(uint32_t (&sv)[32], const float4 *nl4, float sl2, int q0, int qmin)
 {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+#pragma unroll
+    for (int e4 = 0; e4 < 8; ++e4) {
+        const float4 lz = nl4[e4];
+        float p0, p1, p2, p3;
+        ffma2(p0, p1, __uint_as_float(sv[4 * e4]), __uint_as_float(sv[4 * e4 + 1]), sl2, sl2, lz.x, lz.y);
+        ffma2(p2, p3, __uint_as_float(sv[4 * e4 + 2]), __uint_as_float(sv[4 * e4 + 3]), sl2, sl2, lz.z, lz.w);
+        p0 = ex2_approx(p0);
+        p1 = ex2_approx(p1);
+        p2 = ex2_approx(p2);
+        p3 = ex2_approx(p3);
+        if (MASK) {
+            const int q = q0 + 4 * e4;
+            p0 = q >= qmin ? p0 : 0.f;
+            p1 = q + 1 >= qmin ? p1 : 0.f;
+            p2 = q + 2 >= qmin ? p2 : 0.f;
+            p3 = q + 3 >= qmin ? p3 : 0.f;
+        }
+        sv[4 * e4] = __float_as_uint(p0);
+        sv[4 * e4 + 1] = __float_as_uint(p1);
+        sv[4 * e4 + 2] = __float_as_uint(p2);
+        sv[4 * e4 + 3] = __float_as_uint(p3);
+    }
 }
 
 template <int D>
@@ -160,7 +181,7 @@ __global__ void __launch_bounds__(512, 1)
                     const BwdArgs a)
 {
     using L = BwdLayout<D>;
-    constexpr int BQ = L::BQ;
+    constexpr int NST = L::NST;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -179,15 +200,18 @@ __global__ void __launch_bounds__(512, 1)
             mbar_init(bar(L::B_STEMPTY + s), 1);
         }
         mbar_init(bar(L::B_SFULL), 1);
+        mbar_init(bar(L::B_DPFULL), 1);
         mbar_init(bar(L::B_PFULL), 256);
+        mbar_init(bar(L::B_DSFULL), 256);
         mbar_init(bar(L::B_DVDONE), 1);
-        mbar_init(bar(L::B_DKDONE), 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(L::B_DQFULL + b), 1);
             mbar_init(bar(L::B_DQEMPTY + b), 128);
         }
         mbar_init(bar(L::B_DKVFULL), 1);
         mbar_init(bar(L::B_DKVEMPTY), 128);
+        mbar_init(bar(L::B_LFULL), 1);
+        mbar_init(bar(L::B_DFULL), 1);
         mbar_init(bar(L::B_DRAIN), 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -206,17 +230,22 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t tmem = *tmem_slot;
     const WaitCtx ctx{abort_flag, &g_bwd_status, a.timeout_ns};
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
+    // Register split (launch: 512 threads x 128): the producer/MMA/loader warpgroup gives
+    // 32 per thread to the drain warpgroup, which holds a whole dQ^T tile (128 values per
+    // thread) so that it can return the tensor-memory columns before its atomic adds.
+    // 96 + 128 + 128 + 160 = 4 x 128.
+    if (warp < 4) {
+        regs_dealloc<96>();
+        if (warp == 0 && lane == 0) {
+            // -------------------------------------------------------- producer
             const uint64_t pol_keep = policy_evict_last();
             uint32_t n_kv = 0, n_st = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
-                const Unit x = make_unit<D>(u, a);
+                const Unit x = make_unit(u, a);
                 if (x.nq == 0)
                     continue;
-                if (n_kv > 0 && !mbar_wait(bar(L::B_KVEMPTY), (n_kv - 1) & 1, ctx, SITE_P_KVEMPTY))
+                if (n_kv > 0 && !mbar_wait<true>(bar(L::B_KVEMPTY), (n_kv - 1) & 1, ctx, SITE_P_KVEMPTY))
                     break;
                 mbar_arrive_expect_tx(bar(L::B_KVFULL), 2 * L::KV_TILE);
                 for (int c = 0; c < L::KCH; ++c) {
@@ -226,21 +255,18 @@ __global__ void __launch_bounds__(512, 1)
                 ++n_kv;
                 for (int i = x.i0; i < x.i0 + x.nq; ++i) {
                     const uint32_t s = n_st % NST;
-                    if (n_st >= NST && !mbar_wait(bar(L::B_STEMPTY + s), ((n_st / NST) - 1) & 1, ctx, SITE_P_STEMPTY)) {
+                    if (n_st >= NST && !mbar_wait<true>(bar(L::B_STEMPTY + s), ((n_st / NST) - 1) & 1, ctx, SITE_P_STEMPTY)) {
                         ok = false;
                         break;
                     }
                     const uint32_t st = sbase + L::OFF_ST + s * L::ST_BYTES;
-                    mbar_arrive_expect_tx(bar(L::B_STFULL + s), 2 * L::Q_TILE + 2 * BQ * 4);
+                    mbar_arrive_expect_tx(bar(L::B_STFULL + s), 2 * L::Q_TILE);
                     for (int c = 0; c < L::KCH; ++c) {
                         tma_load_3d_hint(st + L::ST_Q + c * L::Q_CHUNK, &tm_q, bar(L::B_STFULL + s), c * 64, i * BQ,
                                          x.bh, pol_keep);
                         tma_load_3d_hint(st + L::ST_DO + c * L::Q_CHUNK, &tm_do, bar(L::B_STFULL + s), c * 64,
                                          i * BQ, x.bh, pol_keep);
                     }
-                    const size_t roff = (size_t)x.bh * a.Tq_pad + (size_t)i * BQ;
-                    bulk_load(st + L::ST_LSE, a.lse2 + roff, BQ * 4, bar(L::B_STFULL + s));
-                    bulk_load(st + L::ST_D, a.delta + roff, BQ * 4, bar(L::B_STFULL + s));
                     ++n_st;
                 }
             }
@@ -250,116 +276,124 @@ __global__ void __launch_bounds__(512, 1)
                 mbar_wait_drain(bar(L::B_STFULL + i % NST), (i / NST) & 1, a.timeout_ns);
             if (n_kv > 0)
                 mbar_wait_drain(bar(L::B_KVFULL), (n_kv - 1) & 1, a.timeout_ns);
-        }
-        __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        } else if (warp == 1 && lane == 0) {
+            // -------------------------------------------------------- MMA issuer
+        // Per block g the tensor core runs S(g) dP(g)|dV(g) dQ(g) S(g+1) dK(g): dP and dV go
+        // in whichever order their inputs become ready, dQ right after the softmax so that
+        // its drain starts early, and S of the next block before dK so that the next
+        // softmax starts early.  dS(g) in shared memory is rewritten by the softmax of a
+        // later block only after dP of that block has completed, and dP is issued after
+        // dK(g) and dQ(g), so the softmax's wait on dP also covers that hazard.
             uint32_t g = 0, nu = 0;   // global query-block and unit counters of this CTA
             bool ok = true;
             const uint32_t k_s = sbase + L::OFF_K, v_s = sbase + L::OFF_V;
-            auto issue_dq = [&](uint32_t gq) -> bool {
-                const uint32_t b = gq & 1;
-                if (gq >= 2 && !mbar_wait(bar(L::B_DQEMPTY + b), ((gq - 2) >> 1) & 1, ctx, SITE_M_DQEMPTY))
+            const uint64_t kd_k = sdesc_sw128(k_s, 16, 1024), vd_k = sdesc_sw128(v_s, 16, 1024);
+            const uint64_t kd_mn = sdesc_sw128(k_s, L::KV_CHUNK, 1024);
+            auto stage_addr = [&](uint32_t gq) { return sbase + L::OFF_ST + (gq % NST) * L::ST_BYTES; };
+            auto ds_addr = [&](uint32_t gq) { return sbase + L::OFF_DS + (L::NDS == 1 ? 0u : (gq & 1u)) * L::DS_TILE; };
+            // S^T(gq) = K_j Q^T: waits for its stage and for dV(gq-1), the last reader of P^T
+            auto issue_s = [&](uint32_t gq) -> bool {
+                if (!mbar_wait<true>(bar(L::B_STFULL + gq % NST), (gq / NST) & 1, ctx, SITE_M_STFULL))
+                    return false;
+                if (gq > 0 && !mbar_wait<true>(bar(L::B_DVDONE), (gq - 1) & 1, ctx, SITE_M_DVDONE))
                     return false;
                 tc_fence_after();
-                const uint32_t ds = sbase + L::OFF_DS + b * L::DS_TILE;
+                const uint64_t qd_k = sdesc_sw128(stage_addr(gq) + L::ST_Q, 16, 1024);
 #pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk) {
-                    uint64_t ad, bd;
-                    if constexpr (L::DQT) {
-                        // A = K_j^T (M = d, MN-major), B = dS^T (N = queries, MN-major)
-                        ad = sdesc_sw128(k_s + kk * 2048, L::KV_CHUNK, 1024);
-                        bd = sdesc_sw128(ds + kk * 2048, L::DS_CHUNK, 1024);
-                    } else {
-                        // A = dS (M = queries, MN-major), B = K_j (N = d, MN-major)
-                        ad = sdesc_sw128(ds + kk * 2048, L::DS_CHUNK, 1024);
-                        bd = sdesc_sw128(k_s + kk * 2048, L::KV_CHUNK, 1024);
-                    }
-                    mma_ss(tmem + L::T_DQ + b * L::DQ_COLS, ad, bd, L::ID_DQ, kk > 0 ? 1u : 0u);
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t ka = (uint64_t)(((kk >> 2) * L::KV_CHUNK + (kk & 3) * 32) >> 4);
+                    const uint64_t qa = (uint64_t)(((kk >> 2) * L::Q_CHUNK + (kk & 3) * 32) >> 4);
+                    mma_ss(tmem + L::T_S, kd_k + ka, qd_k + qa, L::ID_SDP, kk > 0 ? 1u : 0u);
                 }
-                tc_commit(bar(L::B_DQFULL + b));
+                tc_commit(bar(L::B_SFULL));
                 return true;
             };
             for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
-                const Unit x = make_unit<D>(u, a);
+                const Unit x = make_unit(u, a);
                 if (x.nq == 0)
                     continue;
-                if (!mbar_wait(bar(L::B_KVFULL), nu & 1, ctx, SITE_M_KVFULL))
+                if (!mbar_wait<true>(bar(L::B_KVFULL), nu & 1, ctx, SITE_M_KVFULL) || !issue_s(g))
                     break;
                 for (int i = 0; i < x.nq; ++i, ++g) {
-                    const uint32_t s = g % NST;
-                    if (!mbar_wait(bar(L::B_STFULL + s), (g / NST) & 1, ctx, SITE_M_STFULL)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t st = sbase + L::OFF_ST + s * L::ST_BYTES;
-                    // S^T = K_j Q_i^T overwrites P^T of the previous block: dV(g-1) must be done
-                    if (g > 0 && !mbar_wait(bar(L::B_DVDONE), (g - 1) & 1, ctx, SITE_M_DVDONE)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
+                    const uint32_t st = stage_addr(g);
+                    const uint64_t dod_k = sdesc_sw128(st + L::ST_DO, 16, 1024);
+                    const uint64_t qd_mn = sdesc_sw128(st + L::ST_Q, L::Q_CHUNK, 1024);
+                    const uint64_t dod_mn = sdesc_sw128(st + L::ST_DO, L::Q_CHUNK, 1024);
+                    // dP^T(g) = V_j dO^T (d = 128: into the columns of dQ^T(g-1), after its drain)
+                    // and dV_j += P^T dO (after the softmax's P phase; the first block of a unit
+                    // overwrites the accumulator, after the previous unit's epilogue)
+                    bool dp_done = false, dv_done = false;
+                    PollClock pc;
+                    while (!(dp_done && dv_done)) {
+                        bool progress = false;
+                        if (!dp_done && (!L::DQ_ALIAS || g == 0 || mbar_test(bar(L::B_DQEMPTY), (g - 1) & 1))) {
+                            tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk & 3) * 32;
-                        mma_ss(tmem + L::T_S, sdesc_sw128(k_s + (kk >> 2) * L::KV_CHUNK + off, 16, 1024),
-                               sdesc_sw128(st + L::ST_Q + (kk >> 2) * L::Q_CHUNK + off, 16, 1024), L::ID_SDP,
-                               kk > 0 ? 1u : 0u);
-                    }
-                    // dP^T = V_j dO_i^T overwrites dS^T of the previous block: dK(g-1) must be done
-                    if (g > 0 && !mbar_wait(bar(L::B_DKDONE), (g - 1) & 1, ctx, SITE_M_DKDONE)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
+                            for (int kk = 0; kk < D / 16; ++kk) {
+                                const uint64_t ka = (uint64_t)(((kk >> 2) * L::KV_CHUNK + (kk & 3) * 32) >> 4);
+                                const uint64_t qa = (uint64_t)(((kk >> 2) * L::Q_CHUNK + (kk & 3) * 32) >> 4);
+                                mma_ss(tmem + L::T_DP, vd_k + ka, dod_k + qa, L::ID_SDP, kk > 0 ? 1u : 0u);
+                            }
+                            tc_commit(bar(L::B_DPFULL));
+                            dp_done = progress = true;
+                        }
+                        if (!dv_done && mbar_test(bar(L::B_PFULL), g & 1) &&
+                            (i > 0 || nu == 0 || mbar_test(bar(L::B_DKVEMPTY), (nu - 1) & 1))) {
+                            tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk & 3) * 32;
-                        mma_ss(tmem + L::T_DP, sdesc_sw128(v_s + (kk >> 2) * L::KV_CHUNK + off, 16, 1024),
-                               sdesc_sw128(st + L::ST_DO + (kk >> 2) * L::Q_CHUNK + off, 16, 1024), L::ID_SDP,
-                               kk > 0 ? 1u : 0u);
-                    }
-                    tc_commit(bar(L::B_SFULL));
-                    // dQ of the previous block of this unit runs while the softmax works
-                    if (i > 0 && !issue_dq(g - 1)) {
-                        ok = false;
-                        break;
-                    }
-                    if (!mbar_wait(bar(L::B_PFULL), g & 1, ctx, SITE_M_PFULL)) {
-                        ok = false;
-                        break;
-                    }
-                    if (i == 0 && nu > 0 && !mbar_wait(bar(L::B_DKVEMPTY), (nu - 1) & 1, ctx, SITE_M_DKVEMPTY)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    // dV_j += P^T dO_i ; dK_j += dS^T Q_i  (A from tensor memory, B MN-major)
-#pragma unroll
-                    for (int kk = 0; kk < BQ / 16; ++kk) {
-                        // P^T / dS^T of query columns [16kk, 16kk+16): each softmax warpgroup
-                        // packs its half of the columns at the start of its half of the region
-                        const uint32_t col = (kk < BQ / 32) ? kk * 8 : BQ / 2 + (kk - BQ / 32) * 8;
-                        const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-                        mma_ts(tmem + L::T_DV, tmem + L::T_S + col,
-                               sdesc_sw128(st + L::ST_DO + kk * 2048, L::Q_CHUNK, 1024), L::ID_DKV, acc);
-                    }
-                    tc_commit(bar(L::B_DVDONE));
-#pragma unroll
-                    for (int kk = 0; kk < BQ / 16; ++kk) {
-                        const uint32_t col = (kk < BQ / 32) ? kk * 8 : BQ / 2 + (kk - BQ / 32) * 8;
-                        const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-                        mma_ts(tmem + L::T_DK, tmem + L::T_DP + col,
-                               sdesc_sw128(st + L::ST_Q + kk * 2048, L::Q_CHUNK, 1024), L::ID_DKV, acc);
-                    }
-                    tc_commit(bar(L::B_DKDONE));
-                    tc_commit(bar(L::B_STEMPTY + s));
-                    if (i == x.nq - 1) {
-                        if (!issue_dq(g)) {
+                            for (int kk = 0; kk < BQ / 16; ++kk) {
+                                const uint64_t step = (uint64_t)((kk * 2048) >> 4);
+                                mma_ts(tmem + L::T_DV, tmem + L::T_S + half_packed_col(kk), dod_mn + step, L::ID_DKV,
+                                       (i > 0 || kk > 0) ? 1u : 0u);
+                            }
+                            tc_commit(bar(L::B_DVDONE));
+                            dv_done = progress = true;
+                        }
+                        if (!progress && !poll_continue(pc, ctx, SITE_M_DPDV)) {
                             ok = false;
                             break;
                         }
+                    }
+                    if (!ok)
+                        break;
+                    // dS(g) is in shared memory: dQ, then S of the next block, then dK
+                    if (!mbar_wait<true>(bar(L::B_DSFULL), g & 1, ctx, SITE_M_DSFULL)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t b = L::DQ_ALIAS ? 0u : (g & 1u);
+                    if (!L::DQ_ALIAS && g >= 2 &&
+                        !mbar_wait<true>(bar(L::B_DQEMPTY + b), ((g - 2) >> 1) & 1, ctx, SITE_M_DQEMPTY)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t ds = ds_addr(g);
+                    const uint64_t dsd_mn = sdesc_sw128(ds, L::DS_CHUNK, 1024);
+                    const uint64_t dsd_k = sdesc_sw128(ds, 16, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        const uint64_t step = (uint64_t)((kk * 2048) >> 4);
+                        if constexpr (L::DQ_ALIAS)
+                            mma_ss(tmem + L::T_DQ, kd_mn + step, dsd_mn + step, L::ID_DQ, kk > 0 ? 1u : 0u);
+                        else
+                            mma_ss(tmem + L::T_DQ + b * L::DQ_COLS, dsd_mn + step, kd_mn + step, L::ID_DQ,
+                                   kk > 0 ? 1u : 0u);
+                    }
+                    tc_commit(bar(L::B_DQFULL + b));
+                    if (i + 1 < x.nq && !issue_s(g + 1)) {
+                        ok = false;
+                        break;
+                    }
+                    // dK_j += dS^T Q  (dS^T from shared memory, K-major; Q MN-major)
+#pragma unroll
+                    for (int kk = 0; kk < BQ / 16; ++kk) {
+                        const uint64_t da = (uint64_t)(((kk >> 2) * L::DS_CHUNK + (kk & 3) * 32) >> 4);
+                        const uint64_t step = (uint64_t)((kk * 2048) >> 4);
+                        mma_ss(tmem + L::T_DK, dsd_k + da, qd_mn + step, L::ID_DKV, (i > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc_commit(bar(L::B_STEMPTY + g % NST));
+                    if (i == x.nq - 1) {
                         tc_commit(bar(L::B_DKVFULL));
                         tc_commit(bar(L::B_KVEMPTY));
                     }
@@ -368,88 +402,142 @@ __global__ void __launch_bounds__(512, 1)
             }
             tc_commit(bar(L::B_DRAIN));
             mbar_wait_drain(bar(L::B_DRAIN), 0, a.timeout_ns);
+        } else if (warp == 2 && lane == 0) {
+            // -------------------------------------------------------- lse / D loader
+            // One buffer each: -lse of block g is loaded once the P phase of block g-1 is
+            // done, -D of block g once its dS phase is done.
+            uint32_t g = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+                const Unit x = make_unit(u, a);
+                for (int i = 0; i < x.nq; ++i, ++g) {
+                    const size_t roff = (size_t)x.bh * a.Tq_pad + (size_t)(x.i0 + i) * BQ;
+                    if (g > 0 && !mbar_wait<true>(bar(L::B_PFULL), (g - 1) & 1, ctx, SITE_L_PFULL)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar(L::B_LFULL), BQ * 4);
+                    bulk_load(sbase + L::OFF_LSE, a.nlse2 + roff, BQ * 4, bar(L::B_LFULL));
+                    if (g > 0 && !mbar_wait<true>(bar(L::B_DSFULL), (g - 1) & 1, ctx, SITE_L_DSFULL)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar(L::B_DFULL), BQ * 4);
+                    bulk_load(sbase + L::OFF_DEL, a.ndelta + roff, BQ * 4, bar(L::B_DFULL));
+                }
+            }
+            // copies in flight: the last phase of each buffer that was started
+            if (g > 0) {
+                mbar_wait_drain(bar(L::B_LFULL), (g - 1) & 1, a.timeout_ns);
+                mbar_wait_drain(bar(L::B_DFULL), (g - 1) & 1, a.timeout_ns);
+            }
         }
         __syncwarp();
-    } else if (warp >= 4 && warp < 12) {
+    } else if (warp < 12) {
         // ------------------------------------------------------------ softmax (two warpgroups)
-        const int half = (int)(warp - 4) >> 2;          // query columns [half*BQ/2, (half+1)*BQ/2)
+        const int half = (int)(warp - 4) >> 2;          // query columns [64*half, 64*half + 64)
         const uint32_t quarter = warp & 3u;
         const int key_in_blk = (int)(quarter * 32 + lane);
         const uint32_t lane_base = tmem + ((quarter * 32u) << 16);
-        constexpr int HC = BQ / 2;                      // columns per thread
+        const float sl2 = a.scale_log2;
         uint32_t g = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
-            const Unit x = make_unit<D>(u, a);
+            const Unit x = make_unit(u, a);
             const int l = x.j * BK + key_in_blk;         // this thread's key
             for (int i = 0; i < x.nq; ++i, ++g) {
-                if (!mbar_wait(bar(L::B_SFULL), g & 1, ctx, SITE_S_SFULL)) {
+                const int qb = (x.i0 + i) * BQ + half * 64;        // first query row of this half
+                // column q is allowed iff the key exists and (causal) qb + q >= l - (Tk - Tq)
+                int qmin = l < a.Tk ? 0 : 64;
+                if (a.causal && l < a.Tk) {
+                    const long lim = (long)l - (a.Tk - a.Tq) - qb;
+                    qmin = (int)max(0L, min(64L, lim));
+                }
+                const bool mask = __any_sync(0xffffffffu, qmin > 0);
+                if (!mbar_wait(bar(L::B_SFULL), g & 1, ctx, SITE_S_SFULL) ||
+                    !mbar_wait(bar(L::B_LFULL), g & 1, ctx, SITE_S_LFULL)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t s = g % NST;
-                const float *lse2 = reinterpret_cast<const float *>(smem + L::OFF_ST + s * L::ST_BYTES + L::ST_LSE);
-                const float *dl = reinterpret_cast<const float *>(smem + L::OFF_ST + s * L::ST_BYTES + L::ST_D);
-                const int qb = (x.i0 + i) * BQ;                   // first query row of the block
-                // causal: column q is allowed iff qb + q >= l - (Tk - Tq)
-                int qmin = 0;
-                if (a.causal) {
-                    const long lim = (long)l - (a.Tk - a.Tq) - qb;
-                    qmin = (int)max(0L, min((long)BQ, lim));
+                // P phase: P^T (bf16) over the first half of this warpgroup's own S^T columns
+                uint32_t p0[32], p1[32];
+                tmem_ld_x32_nowait(lane_base + L::T_S + half * 64, p0);
+                tmem_ld_x32_nowait(lane_base + L::T_S + half * 64 + 32, p1);
+                tmem_wait_ld_x32(p0);
+                tmem_wait_ld_x32(p1);
+                const float4 *nl4 = reinterpret_cast<const float4 *>(smem + L::OFF_LSE) + half * 16;
+                if (mask) {
+                    softmax_p32<true>(p0, nl4, sl2, 0, qmin);
+                    softmax_p32<true>(p1, nl4 + 8, sl2, 32, qmin);
+                } else {
+                    softmax_p32<false>(p0, nl4, sl2, 0, 0);
+                    softmax_p32<false>(p1, nl4 + 8, sl2, 32, 0);
                 }
-                uint8_t *ds_row = smem + L::OFF_DS + (g & 1) * L::DS_TILE + key_in_blk * 128;
+                {
+                    uint32_t pk[16];
 #pragma unroll
-                for (int c = 0; c < HC / 32; ++c) {
-                    const int q0 = half * HC + c * 32;          // first query column of this chunk
-                    uint32_t sv[32], dv[32];
-                    tmem_ld_x32(lane_base + L::T_S + q0, sv);
-                    tmem_ld_x32(lane_base + L::T_DP + q0, dv);
-                    uint32_t pk[16], dk[16];
+                    for (int e = 0; e < 16; ++e)
+                        pk[e] = pack_bf16x2(__uint_as_float(p0[2 * e]), __uint_as_float(p0[2 * e + 1]));
+                    tmem_st_x16(lane_base + L::T_S + half * 64, pk);
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        float pr[2], dsv[2];
+                    for (int e = 0; e < 16; ++e)
+                        pk[e] = pack_bf16x2(__uint_as_float(p1[2 * e]), __uint_as_float(p1[2 * e + 1]));
+                    tmem_st_x16(lane_base + L::T_S + half * 64 + 16, pk);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(bar(L::B_PFULL));
+                // dS phase: dS = P o (dP - D) into shared memory ([key][query], 128-byte
+                // swizzle, 64 queries per 128-byte row)
+                if (!mbar_wait(bar(L::B_DPFULL), g & 1, ctx, SITE_S_DPFULL) ||
+                    !mbar_wait(bar(L::B_DFULL), g & 1, ctx, SITE_S_DFULL)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint8_t *ds_row = smem + L::OFF_DS + (L::NDS == 1 ? 0u : (g & 1)) * L::DS_TILE + half * L::DS_CHUNK +
+                                  key_in_blk * 128;
+                const float4 *nd4 = reinterpret_cast<const float4 *>(smem + L::OFF_DEL) + half * 16;
 #pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const int q = q0 + 2 * e + h;
-                            float p = ex2_approx(fmaf(__uint_as_float(sv[2 * e + h]), a.scale_log2, -lse2[q]));
-                            p = (q >= qmin) ? p : 0.f;
-                            pr[h] = p;
-                            dsv[h] = p * (__uint_as_float(dv[2 * e + h]) - dl[q]);
-                        }
-                        pk[e] = pack_bf16x2(pr[0], pr[1]);
-                        dk[e] = pack_bf16x2(dsv[0], dsv[1]);
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t dv[32];
+                    tmem_ld_x32(lane_base + L::T_DP + half * 64 + c * 32, dv);
+                    const uint32_t(&pc_)[32] = c == 0 ? p0 : p1;
+                    uint32_t dk[16];
+#pragma unroll
+                    for (int e4 = 0; e4 < 8; ++e4) {
+                        const float4 dz = nd4[c * 8 + e4];
+                        float t0, t1, t2, t3;
+                        fadd2(t0, t1, __uint_as_float(dv[4 * e4]), __uint_as_float(dv[4 * e4 + 1]), dz.x, dz.y);
+                        fadd2(t2, t3, __uint_as_float(dv[4 * e4 + 2]), __uint_as_float(dv[4 * e4 + 3]), dz.z, dz.w);
+                        fmul2(t0, t1, t0, t1, __uint_as_float(pc_[4 * e4]), __uint_as_float(pc_[4 * e4 + 1]));
+                        fmul2(t2, t3, t2, t3, __uint_as_float(pc_[4 * e4 + 2]), __uint_as_float(pc_[4 * e4 + 3]));
+                        dk[2 * e4] = pack_bf16x2(t0, t1);
+                        dk[2 * e4 + 1] = pack_bf16x2(t2, t3);
                     }
-                    // P^T and dS^T (bf16) over the first half of this warpgroup's columns
-                    const uint32_t tcol = half * HC + c * 16;
-                    tmem_st_x16(lane_base + L::T_S + tcol, pk);
-                    tmem_st_x16(lane_base + L::T_DP + tcol, dk);
-                    // dS^T row of this key into shared memory: [key][query] with 128-byte
-                    // swizzle, 64 queries per 128-byte row chunk
-                    uint8_t *chunk = ds_row + (q0 / 64) * L::DS_CHUNK;
 #pragma unroll
                     for (int v4 = 0; v4 < 4; ++v4) {
-                        const int unit16 = ((q0 % 64) / 8) + v4;
-                        const int sw = unit16 ^ (key_in_blk & 7);
-                        *reinterpret_cast<uint4 *>(chunk + sw * 16) =
+                        const int sw = (c * 4 + v4) ^ (key_in_blk & 7);
+                        *reinterpret_cast<uint4 *>(ds_row + sw * 16) =
                             make_uint4(dk[4 * v4], dk[4 * v4 + 1], dk[4 * v4 + 2], dk[4 * v4 + 3]);
                     }
                 }
-                tmem_wait_st();
                 fence_proxy_async_smem();
                 tc_fence_before();
-                mbar_arrive(bar(L::B_PFULL));
+                mbar_arrive(bar(L::B_DSFULL));
             }
         }
-    } else if (warp >= 12) {
+    } else {
         // ------------------------------------------------------------ dQ drain + dK/dV epilogue
+        regs_alloc<160>();
         const uint32_t quarter = warp & 3u;
         const int row = (int)(quarter * 32 + lane);      // TMEM lane
         const uint32_t lane_base = tmem + ((quarter * 32u) << 16);
         uint32_t g = 0, nu = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
-            const Unit x = make_unit<D>(u, a);
+            const Unit x = make_unit(u, a);
             const int l = x.j * BK + row;
             const size_t krow = (size_t)x.bh * a.Tk + l;
             if (x.nq == 0) {
@@ -464,38 +552,58 @@ __global__ void __launch_bounds__(512, 1)
                 continue;
             }
             for (int i = 0; i < x.nq; ++i, ++g) {
-                const uint32_t b = g & 1;
-                if (!mbar_wait(bar(L::B_DQFULL + b), (g >> 1) & 1, ctx, SITE_D_DQFULL)) {
+                const uint32_t b = L::DQ_ALIAS ? 0u : (g & 1u);
+                const uint32_t ph = L::DQ_ALIAS ? (g & 1u) : ((g >> 1) & 1u);
+                if (!mbar_wait<true>(bar(L::B_DQFULL + b), ph, ctx, SITE_D_DQFULL)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const int qb = (x.i0 + i) * BQ;
                 float *acc = a.dq_acc + ((size_t)x.bh * a.Tq_pad + qb) * D;
-#pragma unroll
-                for (int c = 0; c < L::DQ_COLS / 32; ++c) {
-                    uint32_t v[32];
-                    tmem_ld_x32(lane_base + L::T_DQ + b * L::DQ_COLS + c * 32, v);
-                    if constexpr (L::DQT) {
-                        // lane = feature, column = query: a warp adds 32 consecutive floats per query
+                if constexpr (L::DQ_ALIAS) {
+                    // lane = feature, column = query: a warp adds 32 consecutive floats per
+                    // query.  The whole tile is read into registers first, so the columns go
+                    // back to the MMA before the atomic adds.
+                    uint32_t va[32], vb[32], vc[32], vd[32];
+                    auto add_chunk = [&](const uint32_t(&v)[32], int c) {
 #pragma unroll
                         for (int e = 0; e < 32; ++e)
                             atomicAdd(acc + (size_t)(c * 32 + e) * D + row, __uint_as_float(v[e]));
-                    } else {
-                        // lane = query, column = feature
+                    };
+                    tmem_ld_x32_nowait(lane_base + L::T_DQ, va);
+                    tmem_ld_x32_nowait(lane_base + L::T_DQ + 32, vb);
+                    tmem_ld_x32_nowait(lane_base + L::T_DQ + 64, vc);
+                    tmem_ld_x32_nowait(lane_base + L::T_DQ + 96, vd);
+                    tmem_wait_ld_x32(va);
+                    tmem_wait_ld_x32(vb);
+                    tmem_wait_ld_x32(vc);
+                    tmem_wait_ld_x32(vd);
+                    tc_fence_before();
+                    mbar_arrive(bar(L::B_DQEMPTY));
+                    add_chunk(va, 0);
+                    add_chunk(vb, 1);
+                    add_chunk(vc, 2);
+                    add_chunk(vd, 3);
+                } else {
+                    // lane = query, column = feature
+#pragma unroll
+                    for (int c = 0; c < L::DQ_COLS / 32; ++c) {
+                        uint32_t v[32];
+                        tmem_ld_x32(lane_base + L::T_DQ + b * L::DQ_COLS + c * 32, v);
                         float4 *dst = reinterpret_cast<float4 *>(acc + (size_t)row * D + c * 32);
 #pragma unroll
                         for (int e = 0; e < 8; ++e)
                             atomicAdd(dst + e, make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
                                                            __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3])));
                     }
+                    tc_fence_before();
+                    mbar_arrive(bar(L::B_DQEMPTY + b));
                 }
-                tc_fence_before();
-                mbar_arrive(bar(L::B_DQEMPTY + b));
             }
             if (!ok)
                 break;
-            if (!mbar_wait(bar(L::B_DKVFULL), nu & 1, ctx, SITE_D_DKVFULL))
+            if (!mbar_wait<true>(bar(L::B_DKVFULL), nu & 1, ctx, SITE_D_DKVFULL))
                 break;
             tc_fence_after();
 #pragma unroll
@@ -536,8 +644,9 @@ __global__ void __launch_bounds__(512, 1)
     }
 }
 
-// D_r = dO_r . O_r, lse in log2 units (+inf where no key is allowed or past Tq),
-// and the fp32 dQ accumulator zeroed.  One warp per (padded) row.
+// -D_r = -(dO_r . O_r) and -lse_r in log2 units (-inf where no key is allowed or
+// past Tq), stored negated so that the tile loop adds them; the fp32 dQ
+// accumulator zeroed.  One warp per (padded) row.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__restrict__ o,
                                                       const __nv_bfloat16 *__restrict__ dO,
@@ -578,13 +687,13 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__res
                 dsum += __shfl_xor_sync(0xffffffffu, dsum, off);
         }
         if (lane == 0) {
-            float l2 = INFINITY;
+            float l2 = -INFINITY;
             if (r < Tq) {
                 const float lv = lse[bh * Tq + r];
-                l2 = (lv == -INFINITY) ? INFINITY : lv * 1.4426950408889634f;
+                l2 = (lv == -INFINITY) ? -INFINITY : -lv * 1.4426950408889634f;
             }
             lse2[gr] = l2;
-            delta[gr] = r < Tq ? dsum : 0.f;
+            delta[gr] = r < Tq ? -dsum : 0.f;
         }
         float4 *z = reinterpret_cast<float4 *>(dq_acc + gr * D);
         for (int e = lane; e < D / 4; e += 32)
@@ -641,15 +750,14 @@ int launch_bwd(const void *q, const void *k, const void *v, const void *o, const
         if (st == OK)
             st = encode_tmap_3d(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, Tk, BH, 64, BK);
         if (st == OK)
-            st = encode_tmap_3d(&tq, Tq > 0 ? q : k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, tq_rows, BH, 64, L::BQ);
+            st = encode_tmap_3d(&tq, Tq > 0 ? q : k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, tq_rows, BH, 64, BQ);
         if (st == OK)
-            st = encode_tmap_3d(&tdo, Tq > 0 ? dO : k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, tq_rows, BH, 64,
-                                L::BQ);
+            st = encode_tmap_3d(&tdo, Tq > 0 ? dO : k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, tq_rows, BH, 64, BQ);
         if (st != OK)
             return st;
         BwdArgs a;
-        a.lse2 = ws.lse2;
-        a.delta = ws.delta;
+        a.nlse2 = ws.lse2;
+        a.ndelta = ws.delta;
         a.dq_acc = ws.dq_acc;
         a.dk = static_cast<__nv_bfloat16 *>(dk);
         a.dv = static_cast<__nv_bfloat16 *>(dv);

@@ -71,7 +71,8 @@ struct FwdLayout {
     static constexpr int B_FULL = 0, B_EMPTY = NSLOT, B_QFULL = 2 * NSLOT, B_QEMPTY = 2 * NSLOT + 1,
                          B_SFULL = 2 * NSLOT + 2, B_PFULL = 2 * NSLOT + 4, B_ODONE = 2 * NSLOT + 6,
                          B_OEMPTY = 2 * NSLOT + 8, B_DRAIN = 2 * NSLOT + 10, B_PREAD = 2 * NSLOT + 11,
-                         B_OFINAL = 2 * NSLOT + 13, B_DRAIN1 = 2 * NSLOT + 15, NBAR = 2 * NSLOT + 16;
+                         B_OFINAL = 2 * NSLOT + 13, B_DRAIN1 = 2 * NSLOT + 15, B_TOKEN = 2 * NSLOT + 16,
+                         NBAR = 2 * NSLOT + 18;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;   // tmem base (u32), abort flag (int)
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1024-byte alignment
     static constexpr int S_COL = 0;                  // S buffer b at columns [b*BC, (b+1)*BC)
@@ -86,7 +87,7 @@ struct FwdLayout {
 
 enum WaitSite : int {
     SITE_P_EMPTY = 1, SITE_P_QEMPTY, SITE_M_QFULL, SITE_M_FULL, SITE_M_PFULL, SITE_M_OEMPTY,
-    SITE_S_SFULL, SITE_S_ODONE, SITE_S_EPI, SITE_M_PREAD
+    SITE_S_SFULL, SITE_S_ODONE, SITE_S_EPI, SITE_M_PREAD, SITE_S_TOKEN
 };
 
 struct FwdArgs {
@@ -223,6 +224,8 @@ __global__ void __launch_bounds__(FwdLayout<D>::NTHREADS, 1)
         mbar_init(bar(L::B_OFINAL + 1), 1);
         mbar_init(bar(L::B_DRAIN), 1);
         mbar_init(bar(L::B_DRAIN1), 1);
+        mbar_init(bar(L::B_TOKEN), 128);       // softmax ping-pong: tile 0 done with job j
+        mbar_init(bar(L::B_TOKEN + 1), 128);   //                    tile 1 done with job j
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tm_q);
@@ -496,9 +499,14 @@ __global__ void __launch_bounds__(FwdLayout<D>::NTHREADS, 1)
         const float sl2 = a.scale_log2;
         const uint32_t lane_base = tmem + ((quarter * 32u) << 16);
         uint32_t pv = 0, ep = 0;   // jobs and epilogues of this tile so far
+        // Ping-pong (two tiles): the jobs j < min(n0, n1) of a unit alternate between the two
+        // softmax warpgroups, (0,0), (1,0), (0,1), (1,1), ..., so that one computes while the
+        // other tile's MMAs run.  alt_base counts alternated jobs of earlier units (per tile).
+        uint32_t alt_base = 0;
         for (int u = blockIdx.x; u < a.units; u += gridDim.x) {
             const Plan p = make_plan<D>(u, a);
             const int r = p.row0 + t * BR + rit;
+            const int alt = NQ == 2 ? min(p.n[0], p.n[1]) : 0;
             const bool row_ok = r < a.Tq;
             const size_t grow = (size_t)p.bh * a.Tq + r;
             if (!p.rows[t])
@@ -522,6 +530,16 @@ __global__ void __launch_bounds__(FwdLayout<D>::NTHREADS, 1)
                 if (!mbar_wait(bar(L::B_SFULL + b), ph, ctx, SITE_S_SFULL)) {
                     ok = false;
                     break;
+                }
+                if (NQ == 2 && j < alt && (t == 1 || alt_base + j > 0)) {
+                    // tile 1 waits for tile 0's softmax of the same job; tile 0 waits for tile 1's
+                    // previous alternated job, also across units, so neither token barrier can
+                    // run two phases ahead of its waiter
+                    const uint32_t other = t == 1 ? alt_base + j : alt_base + j - 1;
+                    if (!mbar_wait(bar(L::B_TOKEN + (1 - t)), other & 1, ctx, SITE_S_TOKEN)) {
+                        ok = false;
+                        break;
+                    }
                 }
                 tc_fence_after();
                 // S row: all column chunks in flight, one wait
@@ -607,24 +625,35 @@ __global__ void __launch_bounds__(FwdLayout<D>::NTHREADS, 1)
                         break;
                     }
                     tc_fence_after();
+                    // whole O~ row in flight at once (the S registers are free by now)
+                    constexpr int OCH = D / 32 < 4 ? D / 32 : 4;   // chunks per batch
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t v[32];
-                        const uint32_t ta = lane_base + L::O_COL + t * D + c * 32;
-                        tmem_ld_x32(ta, v);
+                    for (int c0 = 0; c0 < D / 32; c0 += OCH) {
+                        uint32_t ov[OCH][32];
 #pragma unroll
-                        for (int i = 0; i < 32; i += 2) {
-                            float y0, y1;
-                            fmul2(y0, y1, __uint_as_float(v[i]), __uint_as_float(v[i + 1]), alpha, alpha);
-                            v[i] = __float_as_uint(y0);
-                            v[i + 1] = __float_as_uint(y1);
+                        for (int c = 0; c < OCH; ++c)
+                            tmem_ld_x32_nowait(lane_base + L::O_COL + t * D + (c0 + c) * 32, ov[c]);
+#pragma unroll
+                        for (int c = 0; c < OCH; ++c)
+                            tmem_wait_ld_x32(ov[c]);
+#pragma unroll
+                        for (int c = 0; c < OCH; ++c) {
+#pragma unroll
+                            for (int i = 0; i < 32; i += 2) {
+                                float y0, y1;
+                                fmul2(y0, y1, __uint_as_float(ov[c][i]), __uint_as_float(ov[c][i + 1]), alpha, alpha);
+                                ov[c][i] = __float_as_uint(y0);
+                                ov[c][i + 1] = __float_as_uint(y1);
+                            }
+                            tmem_st_x32(lane_base + L::O_COL + t * D + (c0 + c) * 32, ov[c]);
                         }
-                        tmem_st_x32(ta, v);
                     }
                 }
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(bar(L::B_PFULL + b));
+                if (NQ == 2 && j < alt)
+                    mbar_arrive(bar(L::B_TOKEN + t));   // hand the softmax turn to the other tile
                 ++pv;
             }
             if (!ok)
@@ -656,6 +685,7 @@ __global__ void __launch_bounds__(FwdLayout<D>::NTHREADS, 1)
                 a.lse[grow] = l > 0.f ? (m * sl2 + log2f(l)) * 0.69314718055994530942f : -INFINITY;
             tc_fence_before();
             mbar_arrive(bar(L::B_OEMPTY + t));
+            alt_base += alt;
         }
     }
     // ---------------------------------------------------- teardown

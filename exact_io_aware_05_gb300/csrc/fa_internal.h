@@ -31,8 +31,8 @@ int fill_empty_launch(void *o, float *lse, size_t rows, int d, int elem_bytes, c
 
 // Backward workspace; rows of every head are padded to Tq_pad = roundup(Tq, 128).
 struct BwdWorkspace {
-    float *lse2;     // [BH][Tq_pad]    lse * log2(e); +inf for padding rows and rows without keys
-    float *delta;    // [BH][Tq_pad]    D_r = dO_r . O_r (0 for padding rows)
+    float *lse2;     // [BH][Tq_pad]    -lse * log2(e); -inf for padding rows and rows without keys
+    float *delta;    // [BH][Tq_pad]    -D_r = -(dO_r . O_r) (0 for padding rows)
     float *dq_acc;   // [BH][Tq_pad][d] fp32 dQ accumulator (unscaled)
 };
 size_t bwd_row_stride(int Tq);
