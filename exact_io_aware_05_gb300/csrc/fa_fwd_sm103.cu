@@ -24,9 +24,12 @@
 //   * warp 1: a single thread issues every tcgen05.mma and commit;
 //   * one 128-thread softmax warpgroup per query tile (thread = query row =
 //     tensor-memory lane) doing the online softmax and the epilogue;
-//   * the rescale of O~ in tensor memory is skipped for a warp when none of
-//     its 32 rows saw its maximum grow (alpha = 1 exactly), so P~ <= 1 always
-//     and the largest weight of a row is exactly 1.0 in bf16.
+//   * the running maximum that P~, l and O~ refer to moves only when a row's
+//     maximum has grown by more than 2^8 in the exp2 domain (the rescale of
+//     O~ in tensor memory is skipped for a warp when none of its 32 rows needs
+//     it); O~ / l and lse are the same quantities for any reference maximum,
+//     P~ <= 2^8 keeps every sum far from fp32 overflow, and with scores of
+//     unit scale the rescale all but disappears after the first key block.
 //   * every wait is bounded (see fa_common.cuh); on a timeout the CTA drains
 //     its in-flight copies and MMAs, frees tensor memory and returns.
 #include "fa_common.cuh"
@@ -39,6 +42,9 @@ __device__ int g_fwd_status;   // device status word of the forward kernels
 namespace {
 
 constexpr int BR = 128;                 // query rows per tile (= MMA M = TMEM lanes)
+// O~ and l are rescaled to a new row maximum only once it exceeds the one they refer to
+// by more than 2^kRescaleLog2 in the exp2 domain; until then P~ <= 2^kRescaleLog2.
+constexpr float kRescaleLog2 = 8.f;
 
 template <int D>
 struct FwdCfg;
@@ -582,7 +588,7 @@ __global__ void __launch_bounds__(FwdLayout<D>::NTHREADS, 1)
                     mx3 = fmax3(mx3, s[i + 6], s[i + 7]);
                 }
                 const float m_new = fmaxf(m, fmax3(mx0, mx1, fmax3(mx2, mx3, -INFINITY)));
-                const bool resc = (m != -INFINITY) && (m_new > m);
+                const bool resc = (m != -INFINITY) && ((m_new - m) * sl2 > kRescaleLog2);
                 float alpha = 1.f;
                 if (m == -INFINITY) {
                     m = m_new;                     // O~ and l of this row are still exactly 0
