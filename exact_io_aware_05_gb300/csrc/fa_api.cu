@@ -178,7 +178,8 @@ size_t bwd_row_stride(int Tq) { return ((size_t)Tq + 127) / 128 * 128; }
 size_t bwd_workspace_bytes(int BH, int Tq, int d)
 {
     const size_t rows = (size_t)BH * bwd_row_stride(Tq);
-    return 2 * round256(rows * sizeof(float)) + round256(rows * d * sizeof(float));
+    return 2 * round256(rows * sizeof(float)) + round256(rows * d * sizeof(float)) +
+           round256((size_t)BH * 2 * sizeof(float) + rows / 128 * sizeof(int));
 }
 
 BwdWorkspace bwd_workspace_carve(void *ws, int BH, int Tq, int d)
@@ -189,7 +190,9 @@ BwdWorkspace bwd_workspace_carve(void *ws, int BH, int Tq, int d)
     w.lse2 = reinterpret_cast<float *>(p);
     w.delta = reinterpret_cast<float *>(p + round256(rows * sizeof(float)));
     w.dq_acc = reinterpret_cast<float *>(p + 2 * round256(rows * sizeof(float)));
-    (void)d;
+    uint8_t *det = p + 2 * round256(rows * sizeof(float)) + round256(rows * d * sizeof(float));
+    w.kvmax = reinterpret_cast<float *>(det);
+    w.bound = reinterpret_cast<int *>(det + (size_t)BH * 2 * sizeof(float));
     return w;
 }
 
@@ -282,6 +285,14 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
 {
     return bwd_common(q, k, v, o, lse, dO, dq, dk, dv, B, H, Tq, Tk, d, causal, scale, workspace, workspace_bytes, 7,
                       stream);
+}
+
+int fa_bwd_deterministic(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                         const void *dO, void *dq, void *dk, void *dv, int B, int H, int Tq, int Tk, int d,
+                         int causal, float scale, void *workspace, size_t workspace_bytes, fa_stream_t stream)
+{
+    return bwd_common(q, k, v, o, lse, dO, dq, dk, dv, B, H, Tq, Tk, d, causal, scale, workspace, workspace_bytes,
+                      7 | fa::kBwdDeterministic, stream);
 }
 
 int fa_bwd_stage(int stage, const void *q, const void *k, const void *v, const void *o, const float *lse,

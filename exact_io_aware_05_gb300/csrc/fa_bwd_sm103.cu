@@ -100,7 +100,25 @@ struct BwdArgs {
     float scale, scale_log2;
     int nkb, units, group;
     uint64_t timeout_ns;
+    const int *det_bound;   // deterministic mode: per 128-row query block, bound on |dq_acc| (else null)
 };
+
+// Deterministic mode.  dQ_i is a sum over key blocks whose terms arrive in any
+// order; held as int32 fixed point their sum is the same in every order.  The
+// fixed point of query block i is 2^(30 - e) with 2^e above a bound on every
+// partial sum: |sum_l dS_rl K_lc| <= max_l |K_lc| sum_l P_rl |dP_rl - D_r|
+// <= 2 |dO_r|_2 max_l |V_l|_2 max_lc |K_lc|, since the P_rl sum to 1 and
+// |dP_rl|, |D_r| <= |dO_r|_2 max_l |V_l|_2.  The bound's factor-2 headroom
+// below 2^31 absorbs the rounding of each term.
+__device__ __forceinline__ float det_block_scale(int bound_bits)
+{
+    const float B = __int_as_float(bound_bits);
+    if (!(B <= 3.0e38f))
+        return 0.f;                       // non-finite inputs: no meaningful fixed point
+    int e;
+    frexpf(B, &e);                        // B < 2^e (e = 0 for B = 0)
+    return ldexpf(1.f, 30 - max(e, -96));
+}
 
 struct Unit {
     int bh, j;     // head, key block
@@ -561,6 +579,8 @@ __global__ void __launch_bounds__(512, 1)
                 tc_fence_after();
                 const int qb = (x.i0 + i) * BQ;
                 float *acc = a.dq_acc + ((size_t)x.bh * a.Tq_pad + qb) * D;
+                const float dsc = a.det_bound ? det_block_scale(a.det_bound[((size_t)x.bh * a.Tq_pad + qb) / BQ]) : 0.f;
+                int *iacc = reinterpret_cast<int *>(acc);
                 if constexpr (L::DQ_ALIAS) {
                     // lane = feature, column = query: a warp adds 32 consecutive floats per
                     // query.  The whole tile is read into registers first, so the columns go
@@ -581,21 +601,40 @@ __global__ void __launch_bounds__(512, 1)
                     tmem_wait_ld_x32(vd);
                     tc_fence_before();
                     mbar_arrive(bar(L::B_DQEMPTY));
-                    add_chunk(va, 0);
-                    add_chunk(vb, 1);
-                    add_chunk(vc, 2);
-                    add_chunk(vd, 3);
+                    if (a.det_bound) {
+                        auto add_chunk_fixed = [&](const uint32_t(&v)[32], int c) {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                atomicAdd(iacc + (size_t)(c * 32 + e) * D + row, __float2int_rn(__uint_as_float(v[e]) * dsc));
+                        };
+                        add_chunk_fixed(va, 0);
+                        add_chunk_fixed(vb, 1);
+                        add_chunk_fixed(vc, 2);
+                        add_chunk_fixed(vd, 3);
+                    } else {
+                        add_chunk(va, 0);
+                        add_chunk(vb, 1);
+                        add_chunk(vc, 2);
+                        add_chunk(vd, 3);
+                    }
                 } else {
                     // lane = query, column = feature
 #pragma unroll
                     for (int c = 0; c < L::DQ_COLS / 32; ++c) {
                         uint32_t v[32];
                         tmem_ld_x32(lane_base + L::T_DQ + b * L::DQ_COLS + c * 32, v);
-                        float4 *dst = reinterpret_cast<float4 *>(acc + (size_t)row * D + c * 32);
+                        if (a.det_bound) {
+                            int *dst = iacc + (size_t)row * D + c * 32;
 #pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            atomicAdd(dst + e, make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
-                                                           __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3])));
+                            for (int e = 0; e < 32; ++e)
+                                atomicAdd(dst + e, __float2int_rn(__uint_as_float(v[e]) * dsc));
+                        } else {
+                            float4 *dst = reinterpret_cast<float4 *>(acc + (size_t)row * D + c * 32);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                atomicAdd(dst + e, make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                                                               __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3])));
+                        }
                     }
                     tc_fence_before();
                     mbar_arrive(bar(L::B_DQEMPTY + b));
@@ -644,14 +683,50 @@ __global__ void __launch_bounds__(512, 1)
     }
 }
 
+// Deterministic mode, first: per head the largest |V_l|_2 and |K_lc| (float bits,
+// maxima of non-negative values in any order).  One warp per key row.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_kvmax_kernel(const __nv_bfloat16 *__restrict__ k,
+                                                        const __nv_bfloat16 *__restrict__ v, float *__restrict__ kvmax,
+                                                        int BH, int Tk)
+{
+    const size_t rows = (size_t)BH * Tk;
+    const int lane = threadIdx.x & 31;
+    constexpr int PER = D / 32;
+    for (size_t gr = (blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5; gr < rows;
+         gr += ((size_t)gridDim.x * blockDim.x) >> 5) {
+        float ss = 0.f, km = 0.f;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) {
+            const float vv = __bfloat162float(v[gr * D + lane * PER + e]);
+            const float kv = __bfloat162float(k[gr * D + lane * PER + e]);
+            ss = fmaf(vv, vv, ss);
+            km = fmaxf(km, fabsf(kv));
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            km = fmaxf(km, __shfl_xor_sync(0xffffffffu, km, off));
+        }
+        if (lane == 0) {
+            const size_t bh = gr / Tk;
+            atomicMax(reinterpret_cast<int *>(kvmax) + 2 * bh, __float_as_int(sqrtf(ss)));
+            atomicMax(reinterpret_cast<int *>(kvmax) + 2 * bh + 1, __float_as_int(km));
+        }
+    }
+}
+
 // -D_r = -(dO_r . O_r) and -lse_r in log2 units (-inf where no key is allowed or
 // past Tq), stored negated so that the tile loop adds them; the fp32 dQ
-// accumulator zeroed.  One warp per (padded) row.
+// accumulator zeroed; deterministic mode: the fixed-point bound of each query
+// block, max over its rows of 2 |dO_r|_2 max|V|_2 max|K|.  One warp per
+// (padded) row.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__restrict__ o,
                                                       const __nv_bfloat16 *__restrict__ dO,
                                                       const float *__restrict__ lse, float *__restrict__ lse2,
-                                                      float *__restrict__ delta, float *__restrict__ dq_acc, int BH,
+                                                      float *__restrict__ delta, float *__restrict__ dq_acc,
+                                                      const float *__restrict__ kvmax, int *__restrict__ bound, int BH,
                                                       int Tq, int Tq_pad)
 {
     const size_t rows = (size_t)BH * Tq_pad;
@@ -660,7 +735,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__res
          gr += ((size_t)gridDim.x * blockDim.x) >> 5) {
         const size_t bh = gr / Tq_pad;
         const int r = (int)(gr - bh * Tq_pad);
-        float dsum = 0.f;
+        float dsum = 0.f, ss = 0.f;
         if (r < Tq) {
             const size_t src = (bh * Tq + r) * D;
             constexpr int PER = D / 32;   // elements per lane (2 or 4)
@@ -674,6 +749,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__res
                     const float2 a2 = __bfloat1622float2(o2[e]), b2 = __bfloat1622float2(g2[e]);
                     dsum = fmaf(a2.x, b2.x, dsum);
                     dsum = fmaf(a2.y, b2.y, dsum);
+                    ss = fmaf(b2.x, b2.x, ss);
+                    ss = fmaf(b2.y, b2.y, ss);
                 }
             } else {
                 const __nv_bfloat162 ov = *reinterpret_cast<const __nv_bfloat162 *>(o + src + lane * 2);
@@ -681,10 +758,14 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__res
                 const float2 a2 = __bfloat1622float2(ov), b2 = __bfloat1622float2(gv);
                 dsum = fmaf(a2.x, b2.x, dsum);
                 dsum = fmaf(a2.y, b2.y, dsum);
+                ss = fmaf(b2.x, b2.x, ss);
+                ss = fmaf(b2.y, b2.y, ss);
             }
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1)
+            for (int off = 16; off > 0; off >>= 1) {
                 dsum += __shfl_xor_sync(0xffffffffu, dsum, off);
+                ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            }
         }
         if (lane == 0) {
             float l2 = -INFINITY;
@@ -694,6 +775,10 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__res
             }
             lse2[gr] = l2;
             delta[gr] = r < Tq ? -dsum : 0.f;
+            if (bound && r < Tq) {
+                const float bnd = 2.f * sqrtf(ss) * kvmax[2 * bh] * kvmax[2 * bh + 1];
+                atomicMax(bound + (gr >> 7), __float_as_int(bnd));
+            }
         }
         float4 *z = reinterpret_cast<float4 *>(dq_acc + gr * D);
         for (int e = lane; e < D / 4; e += 32)
@@ -704,7 +789,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__res
 // dQ = scale * dq_acc, rounded to bf16.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_dq_kernel(const float *__restrict__ dq_acc, __nv_bfloat16 *__restrict__ dq,
-                                                     int BH, int Tq, int Tq_pad, float scale)
+                                                     const int *__restrict__ bound, int BH, int Tq, int Tq_pad,
+                                                     float scale)
 {
     const size_t n8 = (size_t)BH * Tq * (D / 8);
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
@@ -713,7 +799,15 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float *__restrict__ d
         const size_t bh = row / Tq;
         const int r = (int)(row - bh * Tq);
         const float4 *src = reinterpret_cast<const float4 *>(dq_acc + (bh * Tq_pad + r) * D + c8 * 8);
-        const float4 x0 = src[0], x1 = src[1];
+        float4 x0 = src[0], x1 = src[1];
+        if (bound) {   // int32 fixed point of the row's query block -> float
+            const float sc = det_block_scale(bound[(bh * Tq_pad + r) >> 7]);
+            const float inv = sc > 0.f ? 1.f / sc : 0.f;   // a power of two: exact
+            const int4 *isrc = reinterpret_cast<const int4 *>(src);
+            const int4 i0 = isrc[0], i1 = isrc[1];
+            x0 = make_float4((float)i0.x * inv, (float)i0.y * inv, (float)i0.z * inv, (float)i0.w * inv);
+            x1 = make_float4((float)i1.x * inv, (float)i1.y * inv, (float)i1.z * inv, (float)i1.w * inv);
+        }
         uint4 w;
         w.x = pack_bf16x2(x0.x * scale, x0.y * scale);
         w.y = pack_bf16x2(x0.z * scale, x0.w * scale);
@@ -731,14 +825,28 @@ int launch_bwd(const void *q, const void *k, const void *v, const void *o, const
     using L = BwdLayout<D>;
     const int Tq_pad = (int)bwd_row_stride(Tq);
     const int sms = device_sm_count();
-    // 1. preprocess
+    const bool det = (stages & kBwdDeterministic) != 0;
+    // 1. preprocess (deterministic mode: the K/V maxima first, for the fixed-point bounds)
     if ((stages & 1) && Tq > 0) {
         const size_t rows = (size_t)BH * Tq_pad;
+        if (det) {
+            const size_t det_bytes = (size_t)BH * 2 * sizeof(float) + rows / 128 * sizeof(int);
+            if (cudaMemsetAsync(ws.kvmax, 0, det_bytes, s) != cudaSuccess)
+                return ERR_CUDA;
+            if (Tk > 0) {
+                const size_t kblocks = ((size_t)BH * Tk + 7) / 8;
+                const int kgrid = (int)(kblocks < (size_t)sms * 16 ? kblocks : (size_t)sms * 16);
+                bwd_kvmax_kernel<D><<<kgrid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(k),
+                                                          static_cast<const __nv_bfloat16 *>(v), ws.kvmax, BH, Tk);
+                if (cudaGetLastError() != cudaSuccess)
+                    return ERR_CUDA;
+            }
+        }
         const size_t blocks = (rows + 7) / 8;
         const int grid = (int)(blocks < (size_t)sms * 16 ? blocks : (size_t)sms * 16);
         bwd_pre_kernel<D><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(o),
                                                static_cast<const __nv_bfloat16 *>(dO), lse, ws.lse2, ws.delta,
-                                               ws.dq_acc, BH, Tq, Tq_pad);
+                                               ws.dq_acc, ws.kvmax, det ? ws.bound : nullptr, BH, Tq, Tq_pad);
         if (cudaGetLastError() != cudaSuccess)
             return ERR_CUDA;
     }
@@ -774,6 +882,7 @@ int launch_bwd(const void *q, const void *k, const void *v, const void *o, const
         int gsz = (int)(48.0 * 1024 * 1024 / (bytes_head > 1 ? bytes_head : 1));
         a.group = gsz < 1 ? 1 : (gsz > BH ? BH : gsz);
         a.timeout_ns = wait_timeout_ns();
+        a.det_bound = det ? ws.bound : nullptr;
         if (cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES) !=
             cudaSuccess)
             return ERR_CUDA;
@@ -787,7 +896,8 @@ int launch_bwd(const void *q, const void *k, const void *v, const void *o, const
         const size_t n8 = (size_t)BH * Tq * (D / 8);
         const size_t blocks = (n8 + 255) / 256;
         const int grid = (int)(blocks < (size_t)sms * 8 ? blocks : (size_t)sms * 8);
-        bwd_dq_kernel<D><<<grid, 256, 0, s>>>(ws.dq_acc, static_cast<__nv_bfloat16 *>(dq), BH, Tq, Tq_pad, scale);
+        bwd_dq_kernel<D><<<grid, 256, 0, s>>>(ws.dq_acc, static_cast<__nv_bfloat16 *>(dq), det ? ws.bound : nullptr,
+                                              BH, Tq, Tq_pad, scale);
         if (cudaGetLastError() != cudaSuccess)
             return ERR_CUDA;
     }

@@ -34,12 +34,18 @@ struct BwdWorkspace {
     float *lse2;     // [BH][Tq_pad]    -lse * log2(e); -inf for padding rows and rows without keys
     float *delta;    // [BH][Tq_pad]    -D_r = -(dO_r . O_r) (0 for padding rows)
     float *dq_acc;   // [BH][Tq_pad][d] fp32 dQ accumulator (unscaled)
+    // deterministic mode: dq_acc holds int32 fixed point; per head the largest |V_l|_2
+    // and |K_lc| (float bits), and per 128-row query block a bound on |dq_acc| (float bits)
+    float *kvmax;    // [BH][2]
+    int *bound;      // [BH][Tq_pad / 128]
 };
 size_t bwd_row_stride(int Tq);
 size_t bwd_workspace_bytes(int BH, int Tq, int d);
 BwdWorkspace bwd_workspace_carve(void *ws, int BH, int Tq, int d);
-// stages: bit 0 = preprocess (D, lse2, zero dQ accumulator), bit 1 = tile loop
-// (dK, dV, dQ accumulation), bit 2 = dQ scale-and-round.
+// stages: bit 0 = preprocess (D, lse2, zero dQ accumulator; fixed-point bounds),
+// bit 1 = tile loop (dK, dV, dQ accumulation), bit 2 = dQ scale-and-round;
+// kBwdDeterministic: dQ is accumulated as int32 fixed point (order-independent sums).
+constexpr int kBwdDeterministic = 8;
 int bwd_launch(const void *q, const void *k, const void *v, const void *o, const float *lse,
                const void *dO, void *dq, void *dk, void *dv, int BH, int Tq, int Tk, int d,
                int causal, float scale, const BwdWorkspace &ws, int stages, cudaStream_t s);

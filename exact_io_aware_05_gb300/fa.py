@@ -30,6 +30,8 @@ _lib.fa_bwd_workspace_bytes.argtypes = [_i, _i, _i, _i, _i]
 _lib.fa_bwd_workspace_bytes.restype = _sz
 _lib.fa_bwd.argtypes = [_vp] * 9 + [_i] * 6 + [_f, _vp, _sz, _vp]
 _lib.fa_bwd.restype = _i
+_lib.fa_bwd_deterministic.argtypes = [_vp] * 9 + [_i] * 6 + [_f, _vp, _sz, _vp]
+_lib.fa_bwd_deterministic.restype = _i
 _lib.fa_bwd_stage.argtypes = [_i] + [_vp] * 9 + [_i] * 6 + [_f, _vp, _sz, _vp]
 _lib.fa_bwd_stage.restype = _i
 _lib.fa_bwd_noalloc.argtypes = [_vp] * 9 + [_i] * 6 + [_f, _vp]
@@ -119,6 +121,16 @@ def fa_bwd_workspace_bytes(B: int, H: int, Tq: int, Tk: int, d: int) -> int:
 def fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, causal: bool, scale: float, workspace: torch.Tensor,
            stream=None) -> None:
     """dQ, dK, dV (bf16) from bf16 q, k, v, o, dO and the f32 lse of fa_fwd."""
+    _bwd_call("fa_bwd", q, k, v, o, lse, dO, dq, dk, dv, causal, scale, workspace, stream)
+
+
+def fa_bwd_deterministic(q, k, v, o, lse, dO, dq, dk, dv, causal: bool, scale: float,
+                         workspace: torch.Tensor, stream=None) -> None:
+    """fa_bwd with the dQ additions in a fixed order: dq is bitwise reproducible."""
+    _bwd_call("fa_bwd_deterministic", q, k, v, o, lse, dO, dq, dk, dv, causal, scale, workspace, stream)
+
+
+def _bwd_call(entry, q, k, v, o, lse, dO, dq, dk, dv, causal, scale, workspace, stream):
     B, H, Tq, Tk, d = _shapes(q, k)
     dev = q.device
     for name, t, shp in (("q", q, (B, H, Tq, d)), ("k", k, (B, H, Tk, d)), ("v", v, (B, H, Tk, d)),
@@ -129,9 +141,9 @@ def fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, causal: bool, scale: float, workspac
     if workspace.device != dev or not workspace.is_contiguous():
         raise ValueError("workspace: must be a contiguous tensor on the same device")
     nbytes = workspace.numel() * workspace.element_size()
-    _check("fa_bwd", _lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
-                                 _ptr(dk), _ptr(dv), B, H, Tq, Tk, d, int(bool(causal)), float(scale),
-                                 _ptr(workspace), nbytes, _stream(stream)))
+    _check(entry, getattr(_lib, entry)(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
+                                       _ptr(dk), _ptr(dv), B, H, Tq, Tk, d, int(bool(causal)), float(scale),
+                                       _ptr(workspace), nbytes, _stream(stream)))
 
 
 def fa_bwd_stage(stage: int, q, k, v, o, lse, dO, dq, dk, dv, causal: bool, scale: float,
@@ -178,10 +190,12 @@ def alloc_workspace(B, H, Tq, Tk, d, device) -> torch.Tensor:
     return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
 
 
-def attention_backward(q, k, v, o, lse, dO, causal: bool, scale: float, workspace=None, stream=None):
-    """Allocates dQ, dK, dV (and the workspace if not given) and runs fa_bwd."""
+def attention_backward(q, k, v, o, lse, dO, causal: bool, scale: float, workspace=None, stream=None,
+                       deterministic: bool = False):
+    """Allocates dQ, dK, dV (and the workspace if not given) and runs fa_bwd
+    (fa_bwd_deterministic when `deterministic`)."""
     B, H, Tq, Tk, d = _shapes(q, k)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws = alloc_workspace(B, H, Tq, Tk, d, q.device) if workspace is None else workspace
-    fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, causal, scale, ws, stream)
+    (fa_bwd_deterministic if deterministic else fa_bwd)(q, k, v, o, lse, dO, dq, dk, dv, causal, scale, ws, stream)
     return dq, dk, dv

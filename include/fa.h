@@ -75,11 +75,12 @@ int fa_fwd_f32(const float *q, const float *k, const float *v, float *o, float *
                fa_stream_t stream);
 
 /*
- * Bytes of device workspace fa_bwd needs for these sizes: a log2-domain copy
- * of lse and the row terms D (each [B][H][Tq_pad] f32) and the fp32 dQ
- * accumulator [B][H][Tq_pad][d], where Tq_pad rounds Tq up to a multiple of 128;
- * each region is 256-byte aligned.  Returns 0 for
- * invalid sizes.
+ * Bytes of device workspace fa_bwd and fa_bwd_deterministic need for these
+ * sizes: a log2-domain copy of lse and the row terms D (each [B][H][Tq_pad]
+ * f32), the dQ accumulator [B][H][Tq_pad][d] (f32, or int32 fixed point in
+ * fa_bwd_deterministic), two f32 per head and one int32 per 128-row query
+ * block (the fixed-point bounds), where Tq_pad rounds Tq up to a multiple of
+ * 128; each region is 256-byte aligned.  Returns 0 for invalid sizes.
  */
 size_t fa_bwd_workspace_bytes(int B, int H, int Tq, int Tk, int d);
 
@@ -96,6 +97,26 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
            const void *dO, void *dq, void *dk, void *dv,
            int B, int H, int Tq, int Tk, int d, int causal, float scale,
            void *workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/*
+ * fa_bwd with dq bitwise the same on every run with the same inputs
+ * (zerotofrontier.app "FlashAttention", "The backward pass, derived", "Which
+ * loop goes outside?": dQ_i is a sum over key blocks added by different
+ * thread blocks, and floating-point additions in arrival order make its last
+ * bits vary between runs).  Here the contributions are added as int32 fixed
+ * point, whose sums do not depend on the order: query block i (128 rows) uses
+ * the grid 2^(e-30) where 2^e exceeds the bound 2 |dO_r|_2 max_l |V_l|_2
+ * max |K| of every partial sum of its rows (the rows of P sum to one), so
+ * nothing overflows and each term is rounded to about 1e-9 of that bound.
+ * dk and dv are computed as by fa_bwd.  It costs one more pass over K and V
+ * (the per-head maxima) and the conversions.  Non-finite inputs give no
+ * meaningful dq.  Arguments, workspace, validation and errors are those of
+ * fa_bwd.
+ */
+int fa_bwd_deterministic(const void *q, const void *k, const void *v, const void *o,
+                         const float *lse, const void *dO, void *dq, void *dk, void *dv,
+                         int B, int H, int Tq, int Tk, int d, int causal, float scale,
+                         void *workspace, size_t workspace_bytes, fa_stream_t stream);
 
 /*
  * One stage of fa_bwd, for callers that schedule or time the three kernels

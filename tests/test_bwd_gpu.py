@@ -9,7 +9,7 @@ import torch
 
 import oracle
 from exact_io_aware_05_gb300 import inputs
-from gpu_util import TOL_GRAD, excess_over_output_rounding, heads_of, rows_of, to64
+from gpu_util import TOL_GRAD, check_grads, heads_of, rows_of, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -26,28 +26,6 @@ def run_bwd(fa, w: inputs.Workload, x=None):
     dq, dk, dv = fa.attention_backward(x["q"], x["k"], x["v"], o, lse, x["do"], w.causal, w.scale)
     assert fa.fa_sync_status() == fa.FA_OK
     return x, (dq, dk, dv)
-
-
-def check_grads(w, x, grads, heads, rows=None, keys=None, tol=TOL_GRAD):
-    """Every gradient element within tol of the oracle, beyond half a bf16 ulp of the exact
-    value (the rounding of the bf16 output itself)."""
-    dq, dk, dv = grads
-    worst = {"dq": 0.0, "dk": 0.0, "dv": 0.0}
-    raw = dict(worst)
-    for (b, h) in heads:
-        q, k, v, do = (to64(x[n][b, h]) for n in ("q", "k", "v", "do"))
-        ref = oracle.attention_bwd(q, k, v, do, w.causal, w.scale, rows=rows, keys=keys)
-        pick = {"dq": (dq, rows), "dk": (dk, keys), "dv": (dv, keys)}
-        for n, (t, ix) in pick.items():
-            g = to64(t[b, h]) if ix is None else to64(t[b, h])[ix]
-            assert np.all(np.isfinite(g)), n
-            raw[n] = max(raw[n], float(np.abs(g - ref[n]).max()) if g.size else 0.0)
-            worst[n] = max(worst[n], excess_over_output_rounding(g, ref[n]))
-    print(f"{w.name}: max|err| " + " ".join(f"{n}={raw[n]:.3e}" for n in raw) +
-          " | beyond bf16 output rounding " + " ".join(f"{n}={worst[n]:.3e}" for n in worst))
-    for n in worst:
-        assert worst[n] <= tol, (n, worst, raw)
-    return raw, worst
 
 
 SMALL = [
