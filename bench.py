@@ -381,6 +381,55 @@ def run_ours(args) -> None:
     print(json.dumps(line), flush=True)
 
 
+def run_decode(args) -> None:
+    """Split-KV decode (fa_decode) on one GPU: one query row per sequence against a 32K-token
+    key/value cache, B8 H32 d128.  HBM-bound: the metric is the K/V bytes streamed per second,
+    against the measured HBM copy bandwidth.  A secondary line; the default run is the
+    fwd+bwd workload above."""
+    import torch
+    from exact_io_aware_05_gb300 import fa, inputs
+    w = inputs.WORKLOADS["decode_b8h32_q1_k32768_d128"]
+    torch.cuda.set_device(0)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(w.seed)
+    q = torch.randn(w.shape_q, device="cuda", generator=g).to(torch.bfloat16)
+    k = torch.randn(w.shape_kv, device="cuda", generator=g).to(torch.bfloat16)
+    v = torch.randn(w.shape_kv, device="cuda", generator=g).to(torch.bfloat16)
+    o = torch.empty_like(q)
+    lse = torch.empty(w.shape_q[:3], device="cuda")
+    ws = torch.empty(fa.fa_decode_workspace_bytes(w.B, w.H, w.Tq, w.Tk, w.d), dtype=torch.uint8, device="cuda")
+    kv_bytes = 2 * k.numel() * k.element_size()
+    step_bytes = kv_bytes + 2 * q.numel() * 2 + lse.numel() * 4
+    for _ in range(args.warmup):
+        fa.fa_decode(q, k, v, o, lse, w.causal, w.scale, ws)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(0)
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        fa.fa_decode(q, k, v, o, lse, w.causal, w.scale, ws)
+    e1.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if fa.fa_sync_status() != fa.FA_OK:
+        raise RuntimeError("fa_decode reported a device-side error")
+    ms = e0.elapsed_time(e1) / args.steps
+    gbs = step_bytes / (ms * 1e-3) / 1e9
+    peak = measured_peaks().get("hbm_gbs")
+    line = {"metric": "split-KV decode, K/V bytes streamed per second, bf16 B8 H32 Tq1 Tk32768 d128",
+            "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "Tq": w.Tq, "Tk": w.Tk, "d": w.d,
+                       "causal": w.causal, "l2": "no flush: K and V are 4.3 GB, larger than the 129 MB L2"},
+            "roofline": {"kernel": "decode_kernel + decode_merge_kernel", "bound": "hbm", "achieved": gbs,
+                         "peak": peak, "unit": "GB/s", "frac": (gbs / peak) if peak else None,
+                         "traffic": None, "peak_source": "measured HBM copy bandwidth, MEASURED_PEAKS.json"},
+            "gpu_launches": 2 * args.steps, "clocks": clk}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -390,6 +439,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode", action="store_true",
+                    help="time split-KV decode (B8 H32 Tq1 Tk32768 d128) instead of the fwd+bwd step")
     ap.add_argument("--batch", type=int, default=WORKLOAD["B"],
                     help="batch size (default 8, the benchmark workload; smaller only for profiling)")
     args = ap.parse_args()
@@ -400,6 +451,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.decode:
+        run_decode(args)
     else:
         run_ours(args)
     if dist_info()[2] > 1:

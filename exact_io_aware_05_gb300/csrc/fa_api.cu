@@ -216,6 +216,41 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int
     return fa::fwd_bf16_launch(q, k, v, o, lse, BH, Tq, Tk, d, causal, scale, s);
 }
 
+size_t fa_decode_workspace_bytes(int B, int H, int Tq, int Tk, int d)
+{
+    if (fa::check_sizes(B, H, Tq, Tk, d, 0, 1.f) != fa::OK || Tq > fa::decode_max_rows(d))
+        return 0;
+    const size_t n = fa::decode_workspace_bytes(B * H, Tq, Tk, d);
+    return n > 256 ? n : 256;
+}
+
+int fa_decode(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Tq, int Tk, int d,
+              int causal, float scale, void *workspace, size_t workspace_bytes, fa_stream_t stream)
+{
+    int st = fa::check_fwd(q, k, v, o, lse, B, H, Tq, Tk, d, causal, scale, 2);
+    if (st != fa::OK)
+        return st;
+    if (Tq > fa::decode_max_rows(d))
+        return FA_ERR_UNSUPPORTED;
+    const int BH = B * H;
+    if ((size_t)BH * Tq == 0)
+        return FA_OK;
+    const size_t need = fa::decode_workspace_bytes(BH, Tq, Tk, d);
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+            return FA_ERR_INVALID_ARG;
+        const size_t nq = (size_t)BH * Tq * d * 2, nk = (size_t)BH * Tk * d * 2, nl = (size_t)BH * Tq * sizeof(float);
+        if (fa::overlaps(workspace, need, q, nq) || fa::overlaps(workspace, need, k, nk) ||
+            fa::overlaps(workspace, need, v, nk) || fa::overlaps(workspace, need, o, nq) ||
+            fa::overlaps(workspace, need, lse, nl))
+            return FA_ERR_INVALID_ARG;
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (Tk == 0)
+        return fa::fill_empty_launch(o, lse, (size_t)BH * Tq, d, 2, s);
+    return fa::decode_launch(q, k, v, o, lse, BH, Tq, Tk, d, causal, scale, workspace, s);
+}
+
 int fa_fwd_f32(const float *q, const float *k, const float *v, float *o, float *lse, int B, int H, int Tq, int Tk,
                int d, int causal, float scale, fa_stream_t stream)
 {
@@ -310,10 +345,11 @@ int fa_sync_status(fa_stream_t stream)
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (cudaStreamSynchronize(s) != cudaSuccess)
         return FA_ERR_CUDA;
-    int wf = 0, wb = 0;
-    if (fa::fwd_status_fetch_clear(s, &wf) != fa::OK || fa::bwd_status_fetch_clear(s, &wb) != fa::OK)
+    int wf = 0, wb = 0, wd = 0;
+    if (fa::fwd_status_fetch_clear(s, &wf) != fa::OK || fa::bwd_status_fetch_clear(s, &wb) != fa::OK ||
+        fa::dec_status_fetch_clear(s, &wd) != fa::OK)
         return FA_ERR_CUDA;
-    const int w = wf ? wf : wb;
+    const int w = wf ? wf : (wb ? wb : wd);
     return w ? (w & 0xFF) : FA_OK;
 }
 

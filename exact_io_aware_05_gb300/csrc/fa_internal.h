@@ -50,9 +50,19 @@ int bwd_launch(const void *q, const void *k, const void *v, const void *o, const
                const void *dO, void *dq, void *dk, void *dv, int BH, int Tq, int Tk, int d,
                int causal, float scale, const BwdWorkspace &ws, int stages, cudaStream_t s);
 
+// Split-KV decode (fa_decode_sm103.cu): chunks per head and key tiles per
+// chunk for these sizes, partial-state workspace bytes, query rows allowed per
+// head at head width d, and the launch (split kernel + merge kernel).
+void decode_split(int BH, int Tk, int *nsplit, int *tps);
+size_t decode_workspace_bytes(int BH, int Tq, int Tk, int d);
+int decode_max_rows(int d);
+int decode_launch(const void *q, const void *k, const void *v, void *o, float *lse, int BH, int Tq, int Tk, int d,
+                  int causal, float scale, void *workspace, cudaStream_t s);
+
 // Device status words of the kernel translation units: read, add into *acc
 // the first nonzero value, and clear.  Stream-ordered; the caller syncs.
 int fwd_status_fetch_clear(cudaStream_t s, int *host_word);
 int bwd_status_fetch_clear(cudaStream_t s, int *host_word);
+int dec_status_fetch_clear(cudaStream_t s, int *host_word);
 
 }  // namespace fa

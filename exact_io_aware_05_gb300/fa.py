@@ -26,6 +26,10 @@ _lib.fa_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp
 _lib.fa_fwd.restype = _i
 _lib.fa_fwd_f32.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp]
 _lib.fa_fwd_f32.restype = _i
+_lib.fa_decode.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _sz, _vp]
+_lib.fa_decode.restype = _i
+_lib.fa_decode_workspace_bytes.argtypes = [_i, _i, _i, _i, _i]
+_lib.fa_decode_workspace_bytes.restype = _sz
 _lib.fa_bwd_workspace_bytes.argtypes = [_i, _i, _i, _i, _i]
 _lib.fa_bwd_workspace_bytes.restype = _sz
 _lib.fa_bwd.argtypes = [_vp] * 9 + [_i] * 6 + [_f, _vp, _sz, _vp]
@@ -99,6 +103,39 @@ def fa_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
     _need(lse, "lse", torch.float32, (B, H, Tq), dev)
     _check("fa_fwd", _lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Tq, Tk, d,
                                  int(bool(causal)), float(scale), _stream(stream)))
+
+
+def fa_decode_workspace_bytes(B: int, H: int, Tq: int, Tk: int, d: int) -> int:
+    return int(_lib.fa_decode_workspace_bytes(B, H, Tq, Tk, d))
+
+
+def fa_decode(q, k, v, o, lse, causal: bool, scale: float, workspace: torch.Tensor, stream=None) -> None:
+    """Split-KV O and lse (as fa_fwd) for Tq <= 16 (d = 64, 128) or 8 (d = 256) query rows."""
+    B, H, Tq, Tk, d = _shapes(q, k)
+    dev = q.device
+    _need(q, "q", torch.bfloat16, (B, H, Tq, d), dev)
+    _need(k, "k", torch.bfloat16, (B, H, Tk, d), dev)
+    _need(v, "v", torch.bfloat16, (B, H, Tk, d), dev)
+    _need(o, "o", torch.bfloat16, (B, H, Tq, d), dev)
+    _need(lse, "lse", torch.float32, (B, H, Tq), dev)
+    if workspace.device != dev or not workspace.is_contiguous():
+        raise ValueError("workspace: must be a contiguous tensor on the same device")
+    nbytes = workspace.numel() * workspace.element_size()
+    _check("fa_decode", _lib.fa_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Tq, Tk, d,
+                                       int(bool(causal)), float(scale), _ptr(workspace), nbytes,
+                                       _stream(stream)))
+
+
+def attention_decode(q, k, v, causal: bool, scale: float, workspace=None, stream=None):
+    """Allocates O, lse (and the workspace if not given) and runs fa_decode."""
+    B, H, Tq, Tk, d = _shapes(q, k)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Tq), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        n = fa_decode_workspace_bytes(B, H, Tq, Tk, d)
+        workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
+    fa_decode(q, k, v, o, lse, causal, scale, workspace, stream)
+    return o, lse
 
 
 def fa_fwd_f32(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:

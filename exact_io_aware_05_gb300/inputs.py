@@ -79,6 +79,12 @@ WORKLOADS = {
     "fwdbwd_b1h16_q8192_k65536_d64_causal": Workload("fwdbwd_b1h16_q8192_k65536_d64_causal", 1, 16,
                                                      8192, 65536, 64, True, 1.0 / 8.0,
                                                      torch.bfloat16, seed=5, backward=True),
+    # split-KV decode: one new query row per sequence against a 32K-token key/value cache
+    # (bottom-right causal: the new row sees the whole cache), and 4 rows at 128K keys
+    "decode_b8h32_q1_k32768_d128": Workload("decode_b8h32_q1_k32768_d128", 8, 32, 1, 32768, 128, True,
+                                            1.0 / 128 ** 0.5, torch.bfloat16, seed=6),
+    "decode_b1h32_q4_k131072_d128": Workload("decode_b1h32_q4_k131072_d128", 1, 32, 4, 131072, 128, True,
+                                             1.0 / 128 ** 0.5, torch.bfloat16, seed=7),
 }
 
 

@@ -75,6 +75,26 @@ int fa_fwd_f32(const float *q, const float *k, const float *v, float *o, float *
                fa_stream_t stream);
 
 /*
+ * Split-KV attention for decoding: the O and lse of fa_fwd for a few query
+ * rows per head against a long key/value sequence (atlas.blal.pro
+ * "FlashAttention -- IO-Aware Exact Attention", "Honest caveats & open
+ * questions": one query row leaves the tiled kernel idle; FlashDecoding
+ * splits the keys instead).  Each chunk of 32-key tiles of a head is reduced
+ * to a partial (m, l, O~) per row by the online softmax, and the chunks are
+ * merged by its rescale (zerotofrontier.app "FlashAttention", "The forward
+ * pass", step 2.5).  Same layouts, causal convention (bottom-right), scale
+ * and edge cases as fa_fwd; scores and P stay fp32.  Tq must be at most 16
+ * (d = 64, 128) or 8 (d = 256), else FA_ERR_UNSUPPORTED: use fa_fwd for more
+ * rows.  workspace: at least fa_decode_workspace_bytes(...) bytes, 256-byte
+ * aligned, not overlapping any argument; contents on entry ignored.  The
+ * chunking depends on the sizes only, so results do not depend on the device.
+ */
+size_t fa_decode_workspace_bytes(int B, int H, int Tq, int Tk, int d);   /* 0: invalid or unsupported sizes */
+int fa_decode(const void *q, const void *k, const void *v, void *o, float *lse,
+              int B, int H, int Tq, int Tk, int d, int causal, float scale,
+              void *workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/*
  * Bytes of device workspace fa_bwd and fa_bwd_deterministic need for these
  * sizes: a log2-domain copy of lse and the row terms D (each [B][H][Tq_pad]
  * f32), the dQ accumulator [B][H][Tq_pad][d] (f32, or int32 fixed point in

@@ -91,3 +91,24 @@ def test_bwd_workspace_and_validation(lib):
     assert b(*ptrs, 1, 1, 8, 8, 64, 0, 0.5, p + 65536, 16, None) == 1          # workspace too small
     assert b(*ptrs, 1, 1, 8, 8, 64, 0, 0.5, None, 1 << 20, None) == 1          # no workspace
     assert b(*ptrs, 0, 1, 8, 8, 64, 0, 0.5, None, 0, None) == 0                 # empty
+
+
+def test_decode_workspace_and_validation(lib):
+    lib.fa_decode_workspace_bytes.argtypes = [ctypes.c_int] * 5
+    lib.fa_decode_workspace_bytes.restype = ctypes.c_size_t
+    # 1024 tiles of 32 keys, 256 heads: 8 chunks per head (2048 chunks in all), 130 floats per row state
+    assert lib.fa_decode_workspace_bytes(8, 32, 1, 32768, 128) == 256 * 8 * 1 * 130 * 4
+    # at least 8 tiles a chunk: 4 tiles -> one chunk; 2 rows x 66 floats, rounded up to 256 bytes
+    assert lib.fa_decode_workspace_bytes(1, 1, 2, 100, 64) == 768
+    assert lib.fa_decode_workspace_bytes(1, 1, 17, 64, 128) == 0     # too many query rows
+    assert lib.fa_decode_workspace_bytes(1, 1, 9, 64, 256) == 0
+    assert lib.fa_decode_workspace_bytes(1, 1, 8, 64, 96) == 0       # head width
+    f = lib.fa_decode
+    vp, i, fl, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    f.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, fl, vp, sz, vp]
+    f.restype = i
+    p = 1 << 20   # fake aligned addresses, never dereferenced on these paths
+    args = (p, p + (1 << 16), p + (2 << 16), p + (3 << 16), p + (4 << 16))
+    assert f(*args, 1, 1, 4, 64, 128, 1, float("inf"), p + (5 << 16), 1 << 16, None) == 1
+    assert f(*args, 1, 1, 4, 64, 128, 2, 0.1, p + (5 << 16), 1 << 16, None) == 1      # causal flag
+    assert f(*args, 1, 1, 17, 64, 128, 1, 0.1, p + (5 << 16), 1 << 16, None) in (2, 3)   # no sm_103 here: 3
