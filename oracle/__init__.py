@@ -53,6 +53,13 @@ def _load():
             lib.oracle_bwd.argtypes = [dp, dp, dp, dp, i64, i64, i64, cint, cdbl, ip, i64, ip, i64,
                                        dp, dp, dp, dp, dp, dp, cint]
             lib.oracle_bwd.restype = cint
+            u8p = ctypes.POINTER(ctypes.c_uint8)
+            lib.oracle_fwd_masked.argtypes = [dp, dp, dp, i64, i64, i64, i64, i64, u8p, i64, cdbl, ip, i64,
+                                              dp, dp, cint]
+            lib.oracle_fwd_masked.restype = cint
+            lib.oracle_bwd_masked.argtypes = [dp, dp, dp, dp, i64, i64, i64, i64, i64, u8p, i64, cdbl, ip, i64,
+                                              ip, i64, dp, dp, dp, dp, dp, dp, cint]
+            lib.oracle_bwd_masked.restype = cint
             _lib = lib
     return _lib
 
@@ -75,11 +82,29 @@ def _idx(ix, n) -> np.ndarray:
     return np.ascontiguousarray(np.asarray(ix, dtype=np.int64).reshape(-1))
 
 
-def attention_fwd(q, k, v, causal: bool, scale: float, rows=None, nthreads: int | None = None):
+def _mask_args(causal, window, block_mask, block_size, Tq, Tk):
+    """(left, right, block pointer, block size, keep-alive array) of the C mask: the window
+    (left, right) around the diagonal key r + Tk - Tq replaces `causal` when given (-1 =
+    unbounded side); block_mask [ceil(Tq/bs)][ceil(Tk/bs)], nonzero = allowed."""
+    if window is None:
+        left, right = -1, (0 if causal else -1)
+    else:
+        assert not causal, "give either causal or a window"
+        left, right = int(window[0]), int(window[1])
+    if block_mask is None:
+        return left, right, ctypes.POINTER(ctypes.c_uint8)(), 1, None
+    bm = np.ascontiguousarray(np.asarray(block_mask) != 0, dtype=np.uint8)
+    assert bm.shape == (-(-Tq // block_size), -(-Tk // block_size)), bm.shape
+    return left, right, bm.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)), block_size, bm
+
+
+def attention_fwd(q, k, v, causal: bool, scale: float, rows=None, nthreads: int | None = None,
+                  window=None, block_mask=None, block_size: int = 128):
     """O [len(rows), d] and lse [len(rows)] for one head (q [Tq,d], k/v [Tk,d]).
 
     rows=None evaluates every query row.  Inputs are converted to float64 first,
-    so bf16 inputs enter with exactly their rounded values.
+    so bf16 inputs enter with exactly their rounded values.  window=(left, right)
+    and block_mask select the allowed (row, key) pairs as in attn_oracle.c.
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     Tq, d = q.shape
@@ -89,15 +114,22 @@ def attention_fwd(q, k, v, causal: bool, scale: float, rows=None, nthreads: int 
     o = np.zeros((r.size, d), dtype=np.float64)
     lse = np.zeros(r.size, dtype=np.float64)
     nt = nthreads or default_threads()
-    st = _load().oracle_fwd(_ptr(q), _ptr(k), _ptr(v), Tq, Tk, d, int(bool(causal)), float(scale),
-                            _ptr(r, ctypes.c_int64), r.size, _ptr(o), _ptr(lse), nt)
+    if window is None and block_mask is None:
+        st = _load().oracle_fwd(_ptr(q), _ptr(k), _ptr(v), Tq, Tk, d, int(bool(causal)), float(scale),
+                                _ptr(r, ctypes.c_int64), r.size, _ptr(o), _ptr(lse), nt)
+    else:
+        left, right, bp, bs, keep = _mask_args(causal, window, block_mask, block_size, Tq, Tk)
+        st = _load().oracle_fwd_masked(_ptr(q), _ptr(k), _ptr(v), Tq, Tk, d, left, right, bp, bs, float(scale),
+                                       _ptr(r, ctypes.c_int64), r.size, _ptr(o), _ptr(lse), nt)
+        del keep
     if st:
         raise RuntimeError(f"oracle_fwd failed with status {st}")
     return o, lse
 
 
 def attention_bwd(q, k, v, dO, causal: bool, scale: float, rows=None, keys=None,
-                  want_o: bool = False, nthreads: int | None = None):
+                  want_o: bool = False, nthreads: int | None = None, window=None, block_mask=None,
+                  block_size: int = 128):
     """Analytic gradients of one head.
 
     Returns a dict with dq [len(rows), d], dk and dv [len(keys), d], and the
@@ -118,9 +150,16 @@ def attention_bwd(q, k, v, dO, causal: bool, scale: float, rows=None, keys=None,
     o = np.zeros((Tq, d)) if want_o else None
     nt = nthreads or default_threads()
     o_ptr = _ptr(o) if want_o else ctypes.POINTER(ctypes.c_double)()
-    st = _load().oracle_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), Tq, Tk, d, int(bool(causal)),
-                            float(scale), _ptr(r, ctypes.c_int64), r.size, _ptr(kk, ctypes.c_int64),
-                            kk.size, _ptr(dq), _ptr(dk), _ptr(dv), o_ptr, _ptr(lse), _ptr(D), nt)
+    if window is None and block_mask is None:
+        st = _load().oracle_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), Tq, Tk, d, int(bool(causal)),
+                                float(scale), _ptr(r, ctypes.c_int64), r.size, _ptr(kk, ctypes.c_int64),
+                                kk.size, _ptr(dq), _ptr(dk), _ptr(dv), o_ptr, _ptr(lse), _ptr(D), nt)
+    else:
+        left, right, bp, bs, keep = _mask_args(causal, window, block_mask, block_size, Tq, Tk)
+        st = _load().oracle_bwd_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), Tq, Tk, d, left, right, bp, bs,
+                                       float(scale), _ptr(r, ctypes.c_int64), r.size, _ptr(kk, ctypes.c_int64),
+                                       kk.size, _ptr(dq), _ptr(dk), _ptr(dv), o_ptr, _ptr(lse), _ptr(D), nt)
+        del keep
     if st:
         raise RuntimeError(f"oracle_bwd failed with status {st}")
     out = {"dq": dq, "dk": dk, "dv": dv, "lse": lse, "D": D}

@@ -32,10 +32,19 @@
  * page's identity D_r = dO_r . O_r is checked against it by the tests, not
  * used here.  The factor c on dQ and dK comes from S = c Q K^T.
  *
+ * Masks (zerotofrontier "FlashAttention", "The causal mask, and the tiles
+ * you never visit"; "Dropout, block-sparsity, and other real-kernel
+ * details": sliding windows are functions of (r, l), and a block mask skips
+ * whole tiles): key l is allowed for query r iff
+ *    l >= r + (Tk - Tq) - left    (when left >= 0; -1: no lower bound)
+ *    l <= r + (Tk - Tq) + right   (when right >= 0; -1: no upper bound)
+ *    block[r / bs][l / bs] != 0   (when a block mask is given)
+ * Causal is left = -1, right = 0.
+ *
  * Readings where the pages are silent (each is listed in the design notes):
  *  - causal masks are aligned bottom-right: key l is allowed for query r iff
  *    l <= r + (Tk - Tq); this is the pages' "query r sees keys l <= r" when
- *    Tq == Tk.
+ *    Tq == Tk.  Windows are measured from the same diagonal key.
  *  - a row with no allowed key has O = 0, lse = -inf and zero gradients.
  *
  * Layout: q, o, dO, dq are [Tq][d]; k, v, dk, dv are [Tk][d]; row-major fp64.
@@ -49,9 +58,28 @@
 #include <stdlib.h>
 #include <string.h>
 
-static int is_allowed(int64_t r, int64_t l, int64_t Tq, int64_t Tk, int causal)
+typedef struct {
+    int64_t left, right;     /* window around the diagonal key r + Tk - Tq; -1 = unbounded */
+    const uint8_t *block;    /* NULL, or [ceil(Tq / bs)][ceil(Tk / bs)], nonzero = allowed */
+    int64_t bs;              /* block size of the block mask (rows and keys) */
+} mask_t;
+
+static int is_allowed(int64_t r, int64_t l, int64_t Tq, int64_t Tk, const mask_t *m)
 {
-    return !causal || l <= r + (Tk - Tq);
+    const int64_t diag = r + (Tk - Tq);
+    if (m->right >= 0 && l > diag + m->right)
+        return 0;
+    if (m->left >= 0 && l < diag - m->left)
+        return 0;
+    if (m->block && !m->block[(r / m->bs) * ((Tk + m->bs - 1) / m->bs) + l / m->bs])
+        return 0;
+    return 1;
+}
+
+static mask_t causal_mask(int causal)
+{
+    mask_t m = {-1, causal ? 0 : -1, NULL, 1};
+    return m;
 }
 
 static double dot(const double *a, const double *b, int64_t d)
@@ -68,7 +96,7 @@ static double dot(const double *a, const double *b, int64_t d)
 typedef struct {
     const double *q, *k, *v;
     int64_t Tq, Tk, d;
-    int causal;
+    mask_t mask;
     double scale;
     const int64_t *rows;   /* which query rows to evaluate */
     int64_t nrows;
@@ -85,7 +113,7 @@ static void forward_row(const fwd_task *T, int64_t r, double *p, double *o_r, do
     double m = -INFINITY;
     /* scores s_rl, masked entries are -inf */
     for (int64_t l = 0; l < T->Tk; ++l) {
-        if (is_allowed(r, l, T->Tq, T->Tk, T->causal)) {
+        if (is_allowed(r, l, T->Tq, T->Tk, &T->mask)) {
             p[l] = T->scale * dot(q_r, T->k + l * d, d);
             if (p[l] > m)
                 m = p[l];
@@ -134,10 +162,10 @@ static void *fwd_worker(void *arg)
  * oracle_fwd: O and lse for the listed query rows of one head.
  * Returns 0 on success, nonzero on a bad argument or allocation failure.
  */
-int oracle_fwd(const double *q, const double *k, const double *v,
-               int64_t Tq, int64_t Tk, int64_t d, int causal, double scale,
-               const int64_t *rows, int64_t nrows,
-               double *o, double *lse, int nthreads)
+static int fwd_run(const double *q, const double *k, const double *v,
+                   int64_t Tq, int64_t Tk, int64_t d, mask_t mask, double scale,
+                   const int64_t *rows, int64_t nrows,
+                   double *o, double *lse, int nthreads)
 {
     if (Tq < 0 || Tk < 0 || d < 1 || nrows < 0 || nthreads < 1)
         return 2;
@@ -152,7 +180,7 @@ int oracle_fwd(const double *q, const double *k, const double *v,
         return 1;
     }
     for (int t = 0; t < nthreads; ++t) {
-        fwd_task x = {q, k, v, Tq, Tk, d, causal, scale, rows, nrows, o, lse, nthreads, t, 0};
+        fwd_task x = {q, k, v, Tq, Tk, d, mask, scale, rows, nrows, o, lse, nthreads, t, 0};
         tasks[t] = x;
         pthread_create(&th[t], NULL, fwd_worker, &tasks[t]);
     }
@@ -164,6 +192,30 @@ int oracle_fwd(const double *q, const double *k, const double *v,
     free(tasks);
     free(th);
     return status;
+}
+
+int oracle_fwd(const double *q, const double *k, const double *v,
+               int64_t Tq, int64_t Tk, int64_t d, int causal, double scale,
+               const int64_t *rows, int64_t nrows,
+               double *o, double *lse, int nthreads)
+{
+    return fwd_run(q, k, v, Tq, Tk, d, causal_mask(causal), scale, rows, nrows, o, lse, nthreads);
+}
+
+/*
+ * oracle_fwd_masked: oracle_fwd under the window (left, right) and block
+ * mask (block, bs) described above (block may be NULL).
+ */
+int oracle_fwd_masked(const double *q, const double *k, const double *v,
+                      int64_t Tq, int64_t Tk, int64_t d, int64_t left, int64_t right,
+                      const uint8_t *block, int64_t bs, double scale,
+                      const int64_t *rows, int64_t nrows,
+                      double *o, double *lse, int nthreads)
+{
+    if (left < -1 || right < -1 || (block && bs < 1))
+        return 2;
+    mask_t m = {left, right, block, block ? bs : 1};
+    return fwd_run(q, k, v, Tq, Tk, d, m, scale, rows, nrows, o, lse, nthreads);
 }
 
 /* ------------------------------------------------------------------ */
@@ -178,7 +230,7 @@ int oracle_fwd(const double *q, const double *k, const double *v,
 typedef struct {
     const double *q, *k, *v, *dO;
     int64_t Tq, Tk, d;
-    int causal;
+    mask_t mask;
     double scale;
     const int64_t *row_slot;  /* [Tq]: index into dq, or -1 */
     const int64_t *keys;
@@ -206,7 +258,7 @@ static void *bwd_rows_worker(void *arg)
         const double *do_r = T->dO + r * d;
         double m = -INFINITY;
         for (int64_t l = 0; l < Tk; ++l) {
-            if (is_allowed(r, l, T->Tq, Tk, T->causal)) {
+            if (is_allowed(r, l, T->Tq, Tk, &T->mask)) {
                 p[l] = T->scale * dot(q_r, T->k + l * d, d);
                 if (p[l] > m)
                     m = p[l];
@@ -286,7 +338,7 @@ static void *bwd_keys_worker(void *arg)
             dv_l[c] = 0.0;
         }
         for (int64_t r = 0; r < T->Tq; ++r) {
-            if (!is_allowed(r, l, T->Tq, T->Tk, T->causal) || T->lse_all[r] == -INFINITY)
+            if (!is_allowed(r, l, T->Tq, T->Tk, &T->mask) || T->lse_all[r] == -INFINITY)
                 continue;
             const double *q_r = T->q + r * d;
             const double *do_r = T->dO + r * d;
@@ -311,12 +363,12 @@ static void *bwd_keys_worker(void *arg)
  *   lse_all, D_all [Tq] are always written; o_all [Tq][d] if non-NULL.
  * Returns 0 on success.
  */
-int oracle_bwd(const double *q, const double *k, const double *v, const double *dO,
-               int64_t Tq, int64_t Tk, int64_t d, int causal, double scale,
-               const int64_t *rows, int64_t nrows,
-               const int64_t *keys, int64_t nkeys,
-               double *dq, double *dk, double *dv,
-               double *o_all, double *lse_all, double *D_all, int nthreads)
+static int bwd_run(const double *q, const double *k, const double *v, const double *dO,
+                   int64_t Tq, int64_t Tk, int64_t d, mask_t mask, double scale,
+                   const int64_t *rows, int64_t nrows,
+                   const int64_t *keys, int64_t nkeys,
+                   double *dq, double *dk, double *dv,
+                   double *o_all, double *lse_all, double *D_all, int nthreads)
 {
     if (Tq < 0 || Tk < 0 || d < 1 || nrows < 0 || nkeys < 0 || nthreads < 1)
         return 2;
@@ -348,7 +400,7 @@ int oracle_bwd(const double *q, const double *k, const double *v, const double *
         return status;
     }
     for (int t = 0; t < nthreads; ++t) {
-        bwd_task x = {q, k, v, dO, Tq, Tk, d, causal, scale, row_slot, keys, nkeys,
+        bwd_task x = {q, k, v, dO, Tq, Tk, d, mask, scale, row_slot, keys, nkeys,
                       dq, dk, dv, o_all, lse_all, D_all, nthreads, t, 0};
         tasks[t] = x;
     }
@@ -368,4 +420,31 @@ int oracle_bwd(const double *q, const double *k, const double *v, const double *
     free(tasks);
     free(th);
     return status;
+}
+
+int oracle_bwd(const double *q, const double *k, const double *v, const double *dO,
+               int64_t Tq, int64_t Tk, int64_t d, int causal, double scale,
+               const int64_t *rows, int64_t nrows,
+               const int64_t *keys, int64_t nkeys,
+               double *dq, double *dk, double *dv,
+               double *o_all, double *lse_all, double *D_all, int nthreads)
+{
+    return bwd_run(q, k, v, dO, Tq, Tk, d, causal_mask(causal), scale, rows, nrows, keys, nkeys, dq, dk, dv,
+                   o_all, lse_all, D_all, nthreads);
+}
+
+/* oracle_bwd_masked: oracle_bwd under the window and block mask of oracle_fwd_masked. */
+int oracle_bwd_masked(const double *q, const double *k, const double *v, const double *dO,
+                      int64_t Tq, int64_t Tk, int64_t d, int64_t left, int64_t right,
+                      const uint8_t *block, int64_t bs, double scale,
+                      const int64_t *rows, int64_t nrows,
+                      const int64_t *keys, int64_t nkeys,
+                      double *dq, double *dk, double *dv,
+                      double *o_all, double *lse_all, double *D_all, int nthreads)
+{
+    if (left < -1 || right < -1 || (block && bs < 1))
+        return 2;
+    mask_t m = {left, right, block, block ? bs : 1};
+    return bwd_run(q, k, v, dO, Tq, Tk, d, m, scale, rows, nrows, keys, nkeys, dq, dk, dv,
+                   o_all, lse_all, D_all, nthreads);
 }
