@@ -213,7 +213,32 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (Tk == 0)
         return fa::fill_empty_launch(o, lse, (size_t)BH * Tq, d, 2, s);
-    return fa::fwd_bf16_launch(q, k, v, o, lse, BH, Tq, Tk, d, causal, scale, s);
+    return fa::fwd_bf16_launch(q, k, v, o, lse, BH, Tq, Tk, d, fa::causal_spec(causal), scale, s);
+}
+
+int fa_fwd_masked(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Tq, int Tk,
+                  int d, int window_left, int window_right, const unsigned char *block_mask, int mask_per_head,
+                  float scale, fa_stream_t stream)
+{
+    if (window_left < -1 || window_right < -1 || mask_per_head < 0 || mask_per_head > 1)
+        return FA_ERR_INVALID_ARG;
+    int st = fa::check_fwd(q, k, v, o, lse, B, H, Tq, Tk, d, 0, scale, 2);
+    if (st != fa::OK)
+        return st;
+    const int BH = B * H;
+    if ((size_t)BH * Tq == 0)
+        return FA_OK;
+    if (block_mask) {
+        const size_t nm = (size_t)(mask_per_head ? BH : 1) * ((Tq + 127) / 128) * ((Tk + 127) / 128);
+        const size_t nq = (size_t)BH * Tq * d * 2, nl = (size_t)BH * Tq * sizeof(float);
+        if (fa::overlaps(block_mask, nm, o, nq) || fa::overlaps(block_mask, nm, lse, nl))
+            return FA_ERR_INVALID_ARG;
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (Tk == 0)
+        return fa::fill_empty_launch(o, lse, (size_t)BH * Tq, d, 2, s);
+    const fa::MaskSpec m{window_left, window_right, block_mask, mask_per_head};
+    return fa::fwd_bf16_launch(q, k, v, o, lse, BH, Tq, Tk, d, m, scale, s);
 }
 
 size_t fa_decode_workspace_bytes(int B, int H, int Tq, int Tk, int d)

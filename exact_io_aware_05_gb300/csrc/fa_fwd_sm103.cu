@@ -99,7 +99,14 @@ enum WaitSite : int {
 struct FwdArgs {
     __nv_bfloat16 *o;
     float *lse;
-    int BH, Tq, Tk, causal;
+    int BH, Tq, Tk;
+    // allowed keys of row r: r + Tk - Tq - left <= l <= r + Tk - Tq + right (-1: that side
+    // unbounded; causal is left = -1, right = 0), in 128 x 128 blocks marked by bmask
+    int left, right;
+    const uint8_t *bmask;   // null, or [heads][nqbm][nkbm], nonzero = visit
+    int bm_per_head;        // one mask per head (else one for all heads)
+    int nqbm, nkbm;         // ceil(Tq / 128), ceil(Tk / 128)
+    int masked;             // a left bound or a block mask: the softmax tiles do not alternate
     float scale_log2;    // scale * log2(e)
     int nqb;             // units per head
     int units;           // BH * nqb
@@ -107,15 +114,46 @@ struct FwdArgs {
     uint64_t timeout_ns;
 };
 
-// One unit = NQ consecutive 128-row query tiles of one (b, h).
-struct Plan {
-    int bh, row0;
-    int n[2];       // KV tiles needed by tile t (0: none)
-    int rows[2];    // tile t has at least one query row
-    int J;          // jobs (one S and one PV MMA each) in the unit
+// One unit = NQ consecutive 128-row query tiles of one (b, h).  Tile t visits the KV
+// blocks j in [lo, hi] (its rows' window) whose 128-key block its mask row marks.
+struct TileRange {
+    int lo, hi;              // KV block range (lo > hi: none)
+    const uint8_t *bm;       // mask row of the tile's 128 rows, or null
+    int n;                   // KV blocks the tile visits (0: none)
+    int first, last;         // first and last of them
+    int rows;                // the tile has at least one query row
 };
 
-template <int D>
+struct Plan {
+    int bh, row0;
+    TileRange tr0, tr1;      // tiles 0 and 1
+    int J;                   // jobs (one S and one PV MMA each) in the unit
+    int js, je;              // first and last KV block any tile visits
+};
+
+// Tile t's range, chosen with a select (no run-time array indexing).
+__device__ __forceinline__ TileRange tile_of(const Plan &p, int t) { return t ? p.tr1 : p.tr0; }
+
+template <int BC>
+__device__ __forceinline__ bool tile_active(const TileRange &r, int j)
+{
+    if (!r.rows || j < r.lo || j > r.hi)
+        return false;
+    return !r.bm || r.bm[(j * BC) >> 7] != 0;
+}
+
+// The first KV block at or after j that the tile visits (hi + 1 if none).
+template <int BC>
+__device__ __forceinline__ int next_active(const TileRange &r, int j)
+{
+    while (j <= r.hi && !tile_active<BC>(r, j))
+        ++j;
+    return j;
+}
+
+// MASKED = false: no left bound and no block mask, so every tile visits a prefix
+// 0 .. n-1 of the KV blocks (causal, non-causal, right-bounded windows).
+template <int D, bool MASKED>
 __device__ __forceinline__ Plan make_plan(int u, const FwdArgs &a)
 {
     using L = FwdLayout<D>;
@@ -128,24 +166,85 @@ __device__ __forceinline__ Plan make_plan(int u, const FwdArgs &a)
     p.bh = g * a.group + (w - lvl * heads_here);
     const int qb = a.nqb - 1 - lvl;
     p.row0 = qb * L::NQ * BR;
-    const int nkv = (a.Tk + L::BC - 1) / L::BC;
+    const long off = (long)a.Tk - a.Tq;
     p.J = 0;
+    p.js = 1 << 30;
+    p.je = -1;
+    if constexpr (!MASKED) {
+        const int nkv = (a.Tk + L::BC - 1) / L::BC;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            TileRange tr;
+            const int r_first = p.row0 + t * BR;
+            tr.rows = (t < L::NQ) && (r_first < a.Tq);
+            int n = 0;
+            if (tr.rows) {
+                if (a.right < 0) {
+                    n = nkv;
+                } else {
+                    const long lim = (long)min(r_first + BR - 1, a.Tq - 1) + off + a.right;   // last row's last key
+                    n = lim < 0 ? 0 : min(nkv, (int)(lim / L::BC) + 1);
+                }
+            }
+            tr.lo = tr.first = 0;
+            tr.hi = tr.last = n - 1;
+            tr.bm = nullptr;
+            tr.n = n;
+            p.J += n;
+            if (t == 0)
+                p.tr0 = tr;
+            else
+                p.tr1 = tr;
+        }
+        p.js = 0;
+        p.je = max(p.tr0.n, p.tr1.n) - 1;
+        return p;
+    }
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
+        TileRange tr;
         const int r_first = p.row0 + t * BR;
-        p.rows[t] = (t < L::NQ) && (r_first < a.Tq);
-        int n = 0;
-        if (p.rows[t]) {
-            if (!a.causal) {
-                n = nkv;
-            } else {
-                const int r_last = min(r_first + BR - 1, a.Tq - 1);
-                const long lim = (long)r_last + a.Tk - a.Tq;   // last allowed key of the last row
-                n = lim < 0 ? 0 : min(nkv, (int)(lim / L::BC) + 1);
+        tr.rows = (t < L::NQ) && (r_first < a.Tq);
+        tr.lo = 0;
+        tr.hi = -1;
+        tr.bm = nullptr;
+        if (tr.rows) {
+            const int r_last = min(r_first + BR - 1, a.Tq - 1);
+            // keys any row of the tile may see: from the first row's lowest to the last row's highest
+            const long klo = a.left >= 0 ? max(0L, (long)r_first + off - a.left) : 0L;
+            const long khi = a.right >= 0 ? min((long)a.Tk - 1, (long)r_last + off + a.right) : (long)a.Tk - 1;
+            if (klo <= khi) {
+                tr.lo = (int)(klo / L::BC);
+                tr.hi = (int)(khi / L::BC);
             }
+            if (a.bmask)
+                tr.bm = a.bmask + ((size_t)(a.bm_per_head ? p.bh : 0) * a.nqbm + (r_first >> 7)) * a.nkbm;
         }
-        p.n[t] = n;
-        p.J += n;
+        int n = 0;
+        if (!tr.bm) {
+            n = tr.hi - tr.lo + 1;
+            tr.first = tr.lo;
+            tr.last = tr.hi;
+        } else {
+            tr.first = tr.hi + 1;
+            tr.last = tr.lo - 1;
+            for (int j = tr.lo; j <= tr.hi; ++j)
+                if (tile_active<L::BC>(tr, j)) {
+                    tr.first = min(tr.first, j);
+                    tr.last = j;
+                    ++n;
+                }
+        }
+        tr.n = n > 0 ? n : 0;
+        if (n > 0) {
+            p.js = min(p.js, tr.first);
+            p.je = max(p.je, tr.last);
+        }
+        p.J += tr.n;
+        if (t == 0)
+            p.tr0 = tr;
+        else
+            p.tr1 = tr;
     }
     return p;
 }
@@ -160,14 +259,14 @@ __device__ __forceinline__ void job_of(const Plan &p, int k, int &t, int &j, boo
         j = k;
         first = last = true;
     } else {
-        const int a = min(p.n[0], p.n[1]);
+        const int a = min(p.tr0.n, p.tr1.n);
         if (k < 2 * a) {
             t = k & 1;
             j = k >> 1;
             first = (t == 0);
             last = (t == 1);
         } else {
-            t = (p.n[0] > p.n[1]) ? 0 : 1;
+            t = (p.tr0.n > p.tr1.n) ? 0 : 1;
             j = a + (k - 2 * a);
             first = last = true;
         }
@@ -192,13 +291,14 @@ __device__ __forceinline__ bool walk_ops(int J, FS &&fs, FPV &&fpv)
     return true;
 }
 
-template <int D>
+template <int D, bool MASKED>
 __global__ void __launch_bounds__(FwdLayout<D>::NTHREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdArgs a)
 {
     using L = FwdLayout<D>;
     constexpr int BC = L::BC, NQ = L::NQ, NSLOT = L::NSLOT;
+    constexpr bool INL = MASKED && NQ == 2;   // register split below: bounded waits inlined (no calls)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -250,254 +350,267 @@ __global__ void __launch_bounds__(FwdLayout<D>::NTHREADS, 1)
 
     uint32_t n_loads = 0, n_q = 0;   // producer counters, kept for the drain
 
-    if (warp == 0) {
-        // ------------------------------------------------ TMA producer
-        if (lane == 0) {
-            const uint64_t pol_kv = policy_evict_last();
-            const uint64_t pol_q = policy_evict_first();
-            for (int u = blockIdx.x; u < a.units; u += gridDim.x) {
-                const Plan p = make_plan<D>(u, a);
-                if (p.J == 0)
-                    continue;
-                if (n_q > 0 && !mbar_wait(bar(L::B_QEMPTY), (n_q - 1) & 1, ctx, SITE_P_QEMPTY))
-                    break;
-                uint32_t qbytes = 0;
-                for (int t = 0; t < NQ; ++t)
-                    qbytes += p.n[t] > 0 ? L::Q_TILE : 0;
-                mbar_arrive_expect_tx(bar(L::B_QFULL), qbytes);
-                for (int t = 0; t < NQ; ++t)
-                    if (p.n[t] > 0)
+    // Register split with masks and two query tiles (launch: 384 threads x 168): the
+    // producer/MMA warpgroup keeps 72 per thread, the softmax warpgroups, which carry the
+    // mask state, take 216; 72 + 2 x 216 = 3 x 168.
+    if (warp < 4) {
+        if constexpr (INL)
+            regs_dealloc<72>();
+        if (warp == 0) {
+            // ------------------------------------------------ TMA producer
+            if (lane == 0) {
+                const uint64_t pol_kv = policy_evict_last();
+                const uint64_t pol_q = policy_evict_first();
+                for (int u = blockIdx.x; u < a.units; u += gridDim.x) {
+                    const Plan p = make_plan<D, MASKED>(u, a);
+                    if (p.J == 0)
+                        continue;
+                    if (n_q > 0 && !mbar_wait<INL>(bar(L::B_QEMPTY), (n_q - 1) & 1, ctx, SITE_P_QEMPTY))
+                        break;
+                    uint32_t qbytes = 0;
+                    for (int t = 0; t < NQ; ++t)
+                        qbytes += tile_of(p, t).n > 0 ? L::Q_TILE : 0;
+                    mbar_arrive_expect_tx(bar(L::B_QFULL), qbytes);
+                    for (int t = 0; t < NQ; ++t)
+                        if (tile_of(p, t).n > 0)
+                            for (int c = 0; c < L::KCH; ++c)
+                                tma_load_3d_hint(sbase + L::OFF_Q + t * L::Q_TILE + c * L::Q_CHUNK, &tm_q,
+                                                 bar(L::B_QFULL), c * 64, p.row0 + t * BR, p.bh, pol_q);
+                    ++n_q;
+                    auto load = [&](const CUtensorMap *map, int j) -> bool {
+                        const uint32_t slot = n_loads % NSLOT;
+                        if (n_loads >= NSLOT &&
+                            !mbar_wait<INL>(bar(L::B_EMPTY + slot), ((n_loads / NSLOT) - 1) & 1, ctx, SITE_P_EMPTY))
+                            return false;
+                        mbar_arrive_expect_tx(bar(L::B_FULL + slot), L::KV_TILE);
+                        const uint32_t dst = sbase + L::OFF_SLOT + slot * L::KV_TILE;
                         for (int c = 0; c < L::KCH; ++c)
-                            tma_load_3d_hint(sbase + L::OFF_Q + t * L::Q_TILE + c * L::Q_CHUNK, &tm_q,
-                                             bar(L::B_QFULL), c * 64, p.row0 + t * BR, p.bh, pol_q);
-                ++n_q;
-                auto load = [&](const CUtensorMap *map, int j) -> bool {
-                    const uint32_t slot = n_loads % NSLOT;
-                    if (n_loads >= NSLOT &&
-                        !mbar_wait(bar(L::B_EMPTY + slot), ((n_loads / NSLOT) - 1) & 1, ctx, SITE_P_EMPTY))
-                        return false;
-                    mbar_arrive_expect_tx(bar(L::B_FULL + slot), L::KV_TILE);
-                    const uint32_t dst = sbase + L::OFF_SLOT + slot * L::KV_TILE;
-                    for (int c = 0; c < L::KCH; ++c)
-                        tma_load_3d_hint(dst + c * L::KV_CHUNK, map, bar(L::B_FULL + slot), c * 64,
-                                         j * BC, p.bh, pol_kv);
-                    ++n_loads;
-                    return true;
-                };
+                            tma_load_3d_hint(dst + c * L::KV_CHUNK, map, bar(L::B_FULL + slot), c * 64,
+                                             j * BC, p.bh, pol_kv);
+                        ++n_loads;
+                        return true;
+                    };
+                    bool ok = true;
+                    if constexpr (NQ == 2) {
+                        // each tile's MMA warp consumes K_j, V_j of every block either tile visits,
+                        // in this order
+                        for (int j = p.js; j <= p.je && ok; ++j)
+                            if (!MASKED || tile_active<BC>(p.tr0, j) || tile_active<BC>(p.tr1, j))
+                                ok = load(&tm_k, j) && load(&tm_v, j);
+                    } else {
+                        // one tile: its visited blocks in the MMA order S(0), S(1), PV(0), S(2), ...
+                        int kj = p.tr0.first, vj = p.tr0.first;
+                        ok = walk_ops(
+                            p.J,
+                            [&](int) {
+                                const bool r = load(&tm_k, kj);
+                                kj = next_active<BC>(p.tr0, kj + 1);
+                                return r;
+                            },
+                            [&](int) {
+                                const bool r = load(&tm_v, vj);
+                                vj = next_active<BC>(p.tr0, vj + 1);
+                                return r;
+                            });
+                    }
+                    if (!ok)
+                        break;
+                }
+                // drain: every copy still in flight lands before the CTA exits
+                const uint32_t lo = n_loads > (uint32_t)NSLOT ? n_loads - NSLOT : 0;
+                for (uint32_t i = lo; i < n_loads; ++i)
+                    mbar_wait_drain(bar(L::B_FULL + i % NSLOT), (i / NSLOT) & 1, a.timeout_ns);
+                if (n_q > 0)
+                    mbar_wait_drain(bar(L::B_QFULL), (n_q - 1) & 1, a.timeout_ns);
+            }
+            __syncwarp();
+        } else if (NQ == 2 && (warp == 1 || warp == 2)) {
+            // ------------------------------------------------ MMA issuer of query tile t
+            // One issuing thread per tile: a single thread cannot issue tcgen05.mma fast enough
+            // to keep the tensor core busy with N = 128 products, two interleave.
+            if (lane == 0) {
+                const int t = (int)warp - 1;
+                const uint32_t s_col = L::S_COL + t * BC, o_col = L::O_COL + t * D;
+                const uint32_t qa = sbase + L::OFF_Q + t * L::Q_TILE;
+                const uint32_t drain_bar = bar(t == 0 ? L::B_DRAIN : L::B_DRAIN1);
+                uint32_t ld = 0, q_seen = 0, pvn = 0, epi = 0;
                 bool ok = true;
-                if constexpr (NQ == 2) {
-                    // each tile's MMA warp consumes K_0, V_0, K_1, V_1, ... in this order
-                    const int nmax = max(p.n[0], p.n[1]);
-                    for (int j = 0; j < nmax && ok; ++j)
-                        ok = load(&tm_k, j) && load(&tm_v, j);
-                } else {
-                    ok = walk_ops(
+                for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+                    const Plan p = make_plan<D, MASKED>(u, a);
+                    if (p.J == 0)
+                        continue;
+                    if (!mbar_wait<INL>(bar(L::B_QFULL), q_seen & 1, ctx, SITE_M_QFULL))
+                        break;
+                    ++q_seen;
+                    const TileRange me = tile_of(p, t), other = tile_of(p, 1 - t);
+                    if (me.n == 0)
+                        mbar_arrive(bar(L::B_QEMPTY));      // this tile reads no Q in this unit
+                    for (int j = p.js; j <= p.je; ++j) {
+                        const bool mine = MASKED ? tile_active<BC>(me, j) : j < me.n;
+                        if (MASKED && !mine && !tile_active<BC>(other, j))
+                            continue;                        // no tile visits block j: not loaded
+                        // K_j: S_t = Q_t K_j^T
+                        const uint32_t ks = ld % NSLOT;
+                        if (!mbar_wait<INL>(bar(L::B_FULL + ks), (ld / NSLOT) & 1, ctx, SITE_M_FULL)) {
+                            ok = false;
+                            break;
+                        }
+                        ++ld;
+                        if (mine) {
+                            // S_t overwrites the columns from which the previous PV of this tile
+                            // read P: that PV must have completed
+                            if (pvn > 0 && !mbar_wait<INL>(bar(L::B_ODONE + t), (pvn - 1) & 1, ctx, SITE_M_PREAD)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            const uint32_t ka = sbase + L::OFF_SLOT + ks * L::KV_TILE;
+#pragma unroll
+                            for (int kk = 0; kk < D / 16; ++kk) {
+                                const uint32_t off = (kk & 3) * 32;
+                                mma_ss(tmem + s_col, sdesc_sw128(qa + (kk >> 2) * L::Q_CHUNK + off, 16, 1024),
+                                       sdesc_sw128(ka + (kk >> 2) * L::KV_CHUNK + off, 16, 1024), L::IDESC_S,
+                                       kk > 0 ? 1u : 0u);
+                            }
+                            tc_commit(bar(L::B_SFULL + t));
+                            tc_commit(bar(L::B_EMPTY + ks));
+                            if (j == me.last)
+                                tc_commit(bar(L::B_QEMPTY));
+                        } else {
+                            mbar_arrive(bar(L::B_EMPTY + ks));  // K_j is only for the other tile
+                        }
+                        // V_j: O_t += P_t V_j
+                        const uint32_t vs = ld % NSLOT;
+                        if (!mbar_wait<INL>(bar(L::B_FULL + vs), (ld / NSLOT) & 1, ctx, SITE_M_FULL)) {
+                            ok = false;
+                            break;
+                        }
+                        ++ld;
+                        if (mine) {
+                            if (!mbar_wait<INL>(bar(L::B_PFULL + t), pvn & 1, ctx, SITE_M_PFULL)) {
+                                ok = false;
+                                break;
+                            }
+                            if (j == (MASKED ? me.first : 0) && epi > 0 &&
+                                !mbar_wait<INL>(bar(L::B_OEMPTY + t), (epi - 1) & 1, ctx, SITE_M_OEMPTY)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            const uint32_t va = sbase + L::OFF_SLOT + vs * L::KV_TILE;
+#pragma unroll
+                            for (int kk = 0; kk < BC / 16; ++kk)
+                                mma_ts(tmem + o_col, tmem + s_col + kk * 8, sdesc_sw128(va + kk * 16 * 128, L::KV_CHUNK, 1024),
+                                       L::IDESC_PV, (j != (MASKED ? me.first : 0) || kk > 0) ? 1u : 0u);
+                            tc_commit(bar(L::B_ODONE + t));   // O~ current and P read: one signal
+                            tc_commit(bar(L::B_EMPTY + vs));
+                            ++pvn;
+                            if (j == me.last) {
+                                tc_commit(bar(L::B_OFINAL + t));
+                                ++epi;
+                            }
+                        } else {
+                            mbar_arrive(bar(L::B_EMPTY + vs));
+                        }
+                    }
+                }
+                tc_commit(drain_bar);
+                mbar_wait_drain(drain_bar, 0, a.timeout_ns);
+            }
+            __syncwarp();
+        } else if (NQ == 1 && warp == 1) {
+            // ------------------------------------------------ MMA issuer (one query tile)
+            if (lane == 0) {
+                uint32_t ld = 0, kg = 0, q_seen = 0;
+                uint32_t epi[2] = {0, 0};
+                for (int u = blockIdx.x; u < a.units; u += gridDim.x) {
+                    const Plan p = make_plan<D, MASKED>(u, a);
+                    if (p.J == 0)
+                        continue;
+                    if (!mbar_wait<INL>(bar(L::B_QFULL), q_seen & 1, ctx, SITE_M_QFULL))
+                        break;
+                    ++q_seen;
+                    uint32_t kslot = 0, vslot = 0;
+                    auto acquire = [&](uint32_t &slot) -> bool {
+                        slot = ld % NSLOT;
+                        const bool ok = mbar_wait<INL>(bar(L::B_FULL + slot), (ld / NSLOT) & 1, ctx, SITE_M_FULL);
+                        ++ld;
+                        return ok;
+                    };
+                    const bool ok = walk_ops(
                         p.J,
-                        [&](int k) {
+                        [&](int k) -> bool {
                             int t, j;
                             bool first, last;
                             job_of<NQ>(p, k, t, j, first, last);
-                            return first ? load(&tm_k, j) : true;
+                            if (first && !acquire(kslot))
+                                return false;
+                            const uint32_t b = (kg + k) & 1;
+                            // S overwrites the columns that held P of job (kg + k - 2): that PV
+                            // must have finished reading them
+                            const uint32_t g = kg + k;
+                            if (g >= 2 && !mbar_wait<INL>(bar(L::B_PREAD + b), ((g - 2) >> 1) & 1, ctx, SITE_M_PREAD))
+                                return false;
+                            tc_fence_after();
+                            const uint32_t qa = sbase + L::OFF_Q + t * L::Q_TILE;
+                            const uint32_t ka = sbase + L::OFF_SLOT + kslot * L::KV_TILE;
+#pragma unroll
+                            for (int kk = 0; kk < D / 16; ++kk) {
+                                const uint32_t off = (kk & 3) * 32;   // 16 bf16 = 32 bytes along K
+                                const uint64_t ad = sdesc_sw128(qa + (kk >> 2) * L::Q_CHUNK + off, 16, 1024);
+                                const uint64_t bd = sdesc_sw128(ka + (kk >> 2) * L::KV_CHUNK + off, 16, 1024);
+                                mma_ss(tmem + L::S_COL + b * BC, ad, bd, L::IDESC_S, kk > 0 ? 1u : 0u);
+                            }
+                            tc_commit(bar(L::B_SFULL + b));
+                            if (last)
+                                tc_commit(bar(L::B_EMPTY + kslot));
+                            if (k == p.J - 1)
+                                tc_commit(bar(L::B_QEMPTY));
+                            return true;
                         },
-                        [&](int k) {
+                        [&](int k) -> bool {
                             int t, j;
                             bool first, last;
                             job_of<NQ>(p, k, t, j, first, last);
-                            return first ? load(&tm_v, j) : true;
+                            if (first && !acquire(vslot))
+                                return false;
+                            const uint32_t b = (kg + k) & 1;
+                            if (!mbar_wait<INL>(bar(L::B_PFULL + b), ((kg + k) >> 1) & 1, ctx, SITE_M_PFULL))
+                                return false;
+                            if (j == 0 && epi[t] > 0 &&
+                                !mbar_wait<INL>(bar(L::B_OEMPTY + t), (epi[t] - 1) & 1, ctx, SITE_M_OEMPTY))
+                                return false;
+                            tc_fence_after();
+                            const uint32_t va = sbase + L::OFF_SLOT + vslot * L::KV_TILE;
+#pragma unroll
+                            for (int kk = 0; kk < BC / 16; ++kk) {
+                                const uint64_t bd = sdesc_sw128(va + kk * 16 * 128, L::KV_CHUNK, 1024);
+                                mma_ts(tmem + L::O_COL + t * D, tmem + L::S_COL + b * BC + kk * 8, bd,
+                                       L::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+                            }
+                            tc_commit(bar(L::B_ODONE + t));
+                            tc_commit(bar(L::B_PREAD + b));
+                            if (last)
+                                tc_commit(bar(L::B_EMPTY + vslot));
+                            if (j == tile_of(p, t).n - 1) {   // last PV of this tile in the unit
+                                tc_commit(bar(L::B_OFINAL + t));
+                                ++epi[t];
+                            }
+                            return true;
                         });
-                }
-                if (!ok)
-                    break;
-            }
-            // drain: every copy still in flight lands before the CTA exits
-            const uint32_t lo = n_loads > (uint32_t)NSLOT ? n_loads - NSLOT : 0;
-            for (uint32_t i = lo; i < n_loads; ++i)
-                mbar_wait_drain(bar(L::B_FULL + i % NSLOT), (i / NSLOT) & 1, a.timeout_ns);
-            if (n_q > 0)
-                mbar_wait_drain(bar(L::B_QFULL), (n_q - 1) & 1, a.timeout_ns);
-        }
-        __syncwarp();
-    } else if (NQ == 2 && (warp == 1 || warp == 2)) {
-        // ------------------------------------------------ MMA issuer of query tile t
-        // One issuing thread per tile: a single thread cannot issue tcgen05.mma fast enough
-        // to keep the tensor core busy with N = 128 products, two interleave.
-        if (lane == 0) {
-            const int t = (int)warp - 1;
-            const uint32_t s_col = L::S_COL + t * BC, o_col = L::O_COL + t * D;
-            const uint32_t qa = sbase + L::OFF_Q + t * L::Q_TILE;
-            const uint32_t drain_bar = bar(t == 0 ? L::B_DRAIN : L::B_DRAIN1);
-            uint32_t ld = 0, q_seen = 0, pvn = 0, epi = 0;
-            bool ok = true;
-            for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
-                const Plan p = make_plan<D>(u, a);
-                if (p.J == 0)
-                    continue;
-                if (!mbar_wait(bar(L::B_QFULL), q_seen & 1, ctx, SITE_M_QFULL))
-                    break;
-                ++q_seen;
-                const int nt = p.n[t], nmax = max(p.n[0], p.n[1]);
-                if (nt == 0)
-                    mbar_arrive(bar(L::B_QEMPTY));      // this tile reads no Q in this unit
-                for (int j = 0; j < nmax; ++j) {
-                    // K_j: S_t = Q_t K_j^T
-                    const uint32_t ks = ld % NSLOT;
-                    if (!mbar_wait(bar(L::B_FULL + ks), (ld / NSLOT) & 1, ctx, SITE_M_FULL)) {
-                        ok = false;
+                    if (!ok)
                         break;
-                    }
-                    ++ld;
-                    if (j < nt) {
-                        // S_t overwrites the columns from which the previous PV of this tile
-                        // read P: that PV must have completed
-                        if (pvn > 0 && !mbar_wait(bar(L::B_ODONE + t), (pvn - 1) & 1, ctx, SITE_M_PREAD)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t ka = sbase + L::OFF_SLOT + ks * L::KV_TILE;
-#pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t off = (kk & 3) * 32;
-                            mma_ss(tmem + s_col, sdesc_sw128(qa + (kk >> 2) * L::Q_CHUNK + off, 16, 1024),
-                                   sdesc_sw128(ka + (kk >> 2) * L::KV_CHUNK + off, 16, 1024), L::IDESC_S,
-                                   kk > 0 ? 1u : 0u);
-                        }
-                        tc_commit(bar(L::B_SFULL + t));
-                        tc_commit(bar(L::B_EMPTY + ks));
-                        if (j == nt - 1)
-                            tc_commit(bar(L::B_QEMPTY));
-                    } else {
-                        mbar_arrive(bar(L::B_EMPTY + ks));  // K_j is only for the other tile
-                    }
-                    // V_j: O_t += P_t V_j
-                    const uint32_t vs = ld % NSLOT;
-                    if (!mbar_wait(bar(L::B_FULL + vs), (ld / NSLOT) & 1, ctx, SITE_M_FULL)) {
-                        ok = false;
-                        break;
-                    }
-                    ++ld;
-                    if (j < nt) {
-                        if (!mbar_wait(bar(L::B_PFULL + t), pvn & 1, ctx, SITE_M_PFULL)) {
-                            ok = false;
-                            break;
-                        }
-                        if (j == 0 && epi > 0 &&
-                            !mbar_wait(bar(L::B_OEMPTY + t), (epi - 1) & 1, ctx, SITE_M_OEMPTY)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t va = sbase + L::OFF_SLOT + vs * L::KV_TILE;
-#pragma unroll
-                        for (int kk = 0; kk < BC / 16; ++kk)
-                            mma_ts(tmem + o_col, tmem + s_col + kk * 8, sdesc_sw128(va + kk * 16 * 128, L::KV_CHUNK, 1024),
-                                   L::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
-                        tc_commit(bar(L::B_ODONE + t));   // O~ current and P read: one signal
-                        tc_commit(bar(L::B_EMPTY + vs));
-                        ++pvn;
-                        if (j == nt - 1) {
-                            tc_commit(bar(L::B_OFINAL + t));
-                            ++epi;
-                        }
-                    } else {
-                        mbar_arrive(bar(L::B_EMPTY + vs));
-                    }
+                    kg += p.J;
                 }
+                // drain: all issued MMAs complete before tensor memory is released
+                tc_commit(bar(L::B_DRAIN));
+                mbar_wait_drain(bar(L::B_DRAIN), 0, a.timeout_ns);
             }
-            tc_commit(drain_bar);
-            mbar_wait_drain(drain_bar, 0, a.timeout_ns);
+            __syncwarp();
         }
-        __syncwarp();
-    } else if (NQ == 1 && warp == 1) {
-        // ------------------------------------------------ MMA issuer (one query tile)
-        if (lane == 0) {
-            uint32_t ld = 0, kg = 0, q_seen = 0;
-            uint32_t epi[2] = {0, 0};
-            for (int u = blockIdx.x; u < a.units; u += gridDim.x) {
-                const Plan p = make_plan<D>(u, a);
-                if (p.J == 0)
-                    continue;
-                if (!mbar_wait(bar(L::B_QFULL), q_seen & 1, ctx, SITE_M_QFULL))
-                    break;
-                ++q_seen;
-                uint32_t kslot = 0, vslot = 0;
-                auto acquire = [&](uint32_t &slot) -> bool {
-                    slot = ld % NSLOT;
-                    const bool ok = mbar_wait(bar(L::B_FULL + slot), (ld / NSLOT) & 1, ctx, SITE_M_FULL);
-                    ++ld;
-                    return ok;
-                };
-                const bool ok = walk_ops(
-                    p.J,
-                    [&](int k) -> bool {
-                        int t, j;
-                        bool first, last;
-                        job_of<NQ>(p, k, t, j, first, last);
-                        if (first && !acquire(kslot))
-                            return false;
-                        const uint32_t b = (kg + k) & 1;
-                        // S overwrites the columns that held P of job (kg + k - 2): that PV
-                        // must have finished reading them
-                        const uint32_t g = kg + k;
-                        if (g >= 2 && !mbar_wait(bar(L::B_PREAD + b), ((g - 2) >> 1) & 1, ctx, SITE_M_PREAD))
-                            return false;
-                        tc_fence_after();
-                        const uint32_t qa = sbase + L::OFF_Q + t * L::Q_TILE;
-                        const uint32_t ka = sbase + L::OFF_SLOT + kslot * L::KV_TILE;
-#pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t off = (kk & 3) * 32;   // 16 bf16 = 32 bytes along K
-                            const uint64_t ad = sdesc_sw128(qa + (kk >> 2) * L::Q_CHUNK + off, 16, 1024);
-                            const uint64_t bd = sdesc_sw128(ka + (kk >> 2) * L::KV_CHUNK + off, 16, 1024);
-                            mma_ss(tmem + L::S_COL + b * BC, ad, bd, L::IDESC_S, kk > 0 ? 1u : 0u);
-                        }
-                        tc_commit(bar(L::B_SFULL + b));
-                        if (last)
-                            tc_commit(bar(L::B_EMPTY + kslot));
-                        if (k == p.J - 1)
-                            tc_commit(bar(L::B_QEMPTY));
-                        return true;
-                    },
-                    [&](int k) -> bool {
-                        int t, j;
-                        bool first, last;
-                        job_of<NQ>(p, k, t, j, first, last);
-                        if (first && !acquire(vslot))
-                            return false;
-                        const uint32_t b = (kg + k) & 1;
-                        if (!mbar_wait(bar(L::B_PFULL + b), ((kg + k) >> 1) & 1, ctx, SITE_M_PFULL))
-                            return false;
-                        if (j == 0 && epi[t] > 0 &&
-                            !mbar_wait(bar(L::B_OEMPTY + t), (epi[t] - 1) & 1, ctx, SITE_M_OEMPTY))
-                            return false;
-                        tc_fence_after();
-                        const uint32_t va = sbase + L::OFF_SLOT + vslot * L::KV_TILE;
-#pragma unroll
-                        for (int kk = 0; kk < BC / 16; ++kk) {
-                            const uint64_t bd = sdesc_sw128(va + kk * 16 * 128, L::KV_CHUNK, 1024);
-                            mma_ts(tmem + L::O_COL + t * D, tmem + L::S_COL + b * BC + kk * 8, bd,
-                                   L::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
-                        }
-                        tc_commit(bar(L::B_ODONE + t));
-                        tc_commit(bar(L::B_PREAD + b));
-                        if (last)
-                            tc_commit(bar(L::B_EMPTY + vslot));
-                        if (j == p.n[t] - 1) {   // last PV of this tile in the unit
-                            tc_commit(bar(L::B_OFINAL + t));
-                            ++epi[t];
-                        }
-                        return true;
-                    });
-                if (!ok)
-                    break;
-                kg += p.J;
-            }
-            // drain: all issued MMAs complete before tensor memory is released
-            tc_commit(bar(L::B_DRAIN));
-            mbar_wait_drain(bar(L::B_DRAIN), 0, a.timeout_ns);
-        }
-        __syncwarp();
-    } else if (warp >= 4) {
+    } else {
+        if constexpr (INL)
+            regs_alloc<216>();
         // ------------------------------------------------ softmax + epilogue
         const int t = (int)(warp - 4) >> 2;            // query tile of this warpgroup
         const uint32_t quarter = warp & 3u;            // TMEM lanes [32*quarter, +32)
@@ -505,19 +618,21 @@ __global__ void __launch_bounds__(FwdLayout<D>::NTHREADS, 1)
         const float sl2 = a.scale_log2;
         const uint32_t lane_base = tmem + ((quarter * 32u) << 16);
         uint32_t pv = 0, ep = 0;   // jobs and epilogues of this tile so far
-        // Ping-pong (two tiles): the jobs j < min(n0, n1) of a unit alternate between the two
-        // softmax warpgroups, (0,0), (1,0), (0,1), (1,1), ..., so that one computes while the
-        // other tile's MMAs run.  alt_base counts alternated jobs of earlier units (per tile).
+        // Ping-pong (two tiles, no left bound or block mask, so both tiles visit a prefix of
+        // the KV blocks): the jobs j < min(n0, n1) of a unit alternate between the two softmax
+        // warpgroups, (0,0), (1,0), (0,1), (1,1), ..., so that one computes while the other
+        // tile's MMAs run.  alt_base counts alternated jobs of earlier units (per tile).
         uint32_t alt_base = 0;
         for (int u = blockIdx.x; u < a.units; u += gridDim.x) {
-            const Plan p = make_plan<D>(u, a);
+            const Plan p = make_plan<D, MASKED>(u, a);
             const int r = p.row0 + t * BR + rit;
-            const int alt = NQ == 2 ? min(p.n[0], p.n[1]) : 0;
+            const TileRange me = tile_of(p, t);
+            const int alt = (NQ == 2 && !a.masked) ? min(p.tr0.n, p.tr1.n) : 0;
             const bool row_ok = r < a.Tq;
             const size_t grow = (size_t)p.bh * a.Tq + r;
-            if (!p.rows[t])
+            if (!me.rows)
                 continue;
-            if (p.n[t] == 0) {   // no key is allowed for any row of this tile
+            if (me.n == 0) {   // no key is allowed for any row of this tile
                 if (row_ok) {
                     uint4 *dst = reinterpret_cast<uint4 *>(a.o + grow * D);
                     for (int i = 0; i < D / 8; ++i)
@@ -528,21 +643,23 @@ __global__ void __launch_bounds__(FwdLayout<D>::NTHREADS, 1)
             }
             float m = -INFINITY, l = 0.f;
             bool ok = true;
-            for (int j = 0; j < p.n[t] && ok; ++j) {
+            // jj: job index of this tile; j: the KV block it visits
+            for (int jj = 0, j = MASKED ? me.first : 0; jj < me.n && ok;
+                 ++jj, j = MASKED ? next_active<BC>(me, j + 1) : jj) {
                 // two tiles: S buffer t, one phase per job of this tile; one tile: the two
                 // S buffers alternate between consecutive jobs
                 const uint32_t b = NQ == 2 ? (uint32_t)t : (pv & 1);
                 const uint32_t ph = NQ == 2 ? (pv & 1) : ((pv >> 1) & 1);
-                if (!mbar_wait(bar(L::B_SFULL + b), ph, ctx, SITE_S_SFULL)) {
+                if (!mbar_wait<INL>(bar(L::B_SFULL + b), ph, ctx, SITE_S_SFULL)) {
                     ok = false;
                     break;
                 }
-                if (NQ == 2 && j < alt && (t == 1 || alt_base + j > 0)) {
+                if (NQ == 2 && jj < alt && (t == 1 || alt_base + jj > 0)) {
                     // tile 1 waits for tile 0's softmax of the same job; tile 0 waits for tile 1's
                     // previous alternated job, also across units, so neither token barrier can
                     // run two phases ahead of its waiter
-                    const uint32_t other = t == 1 ? alt_base + j : alt_base + j - 1;
-                    if (!mbar_wait(bar(L::B_TOKEN + (1 - t)), other & 1, ctx, SITE_S_TOKEN)) {
+                    const uint32_t other = t == 1 ? alt_base + jj : alt_base + jj - 1;
+                    if (!mbar_wait<INL>(bar(L::B_TOKEN + (1 - t)), other & 1, ctx, SITE_S_TOKEN)) {
                         ok = false;
                         break;
                     }
@@ -562,19 +679,25 @@ __global__ void __launch_bounds__(FwdLayout<D>::NTHREADS, 1)
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         s[c * 32 + i] = __uint_as_float(sv[c][i]);
-                // mask: tail keys beyond Tk, and keys after the causal limit
+                // mask: tail keys beyond Tk, and keys outside the row's window (causal: after
+                // its diagonal key), only where the block is not wholly inside every row's window
                 const int kv0 = j * BC;
                 const int first_row = p.row0 + t * BR;
+                const int last_row = min(first_row + BR - 1, a.Tq - 1);
+                const long off = (long)a.Tk - a.Tq;
                 const bool need_mask = (kv0 + BC > a.Tk) ||
-                                       (a.causal && (long)kv0 + BC - 1 > (long)first_row + a.Tk - a.Tq);
+                                       (a.right >= 0 && (long)kv0 + BC - 1 > (long)first_row + off + a.right) ||
+                                       (MASKED && a.left >= 0 && (long)kv0 < (long)last_row + off - a.left);
                 if (need_mask) {
-                    long lim = a.Tk;
-                    if (a.causal)
-                        lim = min(lim, (long)r + a.Tk - a.Tq + 1);
-                    const int cl = (int)max(0L, min((long)BC, lim - kv0));   // columns < cl are allowed
+                    long hi = a.Tk;   // allowed keys of row r: [lo, hi)
+                    if (a.right >= 0)
+                        hi = min(hi, (long)r + off + a.right + 1);
+                    const long lo = (MASKED && a.left >= 0) ? (long)r + off - a.left : 0L;
+                    const int ch = (int)max(0L, min((long)BC, hi - kv0));
+                    const int cl = MASKED ? (int)max(0L, min((long)BC, lo - kv0)) : 0;
 #pragma unroll
                     for (int i = 0; i < BC; ++i)
-                        if (i >= cl)
+                        if (i < cl || i >= ch)
                             s[i] = -INFINITY;
                 }
                 // row max: four independent chains of three-input max
@@ -626,7 +749,7 @@ __global__ void __launch_bounds__(FwdLayout<D>::NTHREADS, 1)
                 l += l0 + l1;
                 if (__any_sync(0xffffffffu, resc)) {
                     // O~ must hold the previous PV of this tile before it is rescaled
-                    if (!mbar_wait(bar(L::B_ODONE + t), (pv - 1) & 1, ctx, SITE_S_ODONE)) {
+                    if (!mbar_wait<INL>(bar(L::B_ODONE + t), (pv - 1) & 1, ctx, SITE_S_ODONE)) {
                         ok = false;
                         break;
                     }
@@ -658,7 +781,7 @@ __global__ void __launch_bounds__(FwdLayout<D>::NTHREADS, 1)
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(bar(L::B_PFULL + b));
-                if (NQ == 2 && j < alt)
+                if (NQ == 2 && jj < alt)
                     mbar_arrive(bar(L::B_TOKEN + t));   // hand the softmax turn to the other tile
                 ++pv;
             }
@@ -667,7 +790,7 @@ __global__ void __launch_bounds__(FwdLayout<D>::NTHREADS, 1)
             // epilogue: O = O~ / l, lse = c m + ln l.  The softmax can be up to two PVs
             // ahead of the tensor core here, too far for a parity wait on the per-PV
             // barrier; the per-unit barrier completes exactly once per epilogue.
-            if (!mbar_wait(bar(L::B_OFINAL + t), ep & 1, ctx, SITE_S_EPI))
+            if (!mbar_wait<INL>(bar(L::B_OFINAL + t), ep & 1, ctx, SITE_S_EPI))
                 break;
             ++ep;
             tc_fence_after();
@@ -705,7 +828,7 @@ __global__ void __launch_bounds__(FwdLayout<D>::NTHREADS, 1)
 
 template <int D>
 int launch(const void *q, const void *k, const void *v, void *o, float *lse, int BH, int Tq, int Tk,
-           int causal, float scale, cudaStream_t s)
+           const MaskSpec &mask, float scale, cudaStream_t s)
 {
     using L = FwdLayout<D>;
     CUtensorMap tq, tk, tv;
@@ -722,7 +845,13 @@ int launch(const void *q, const void *k, const void *v, void *o, float *lse, int
     a.BH = BH;
     a.Tq = Tq;
     a.Tk = Tk;
-    a.causal = causal;
+    a.left = mask.left;
+    a.right = mask.right;
+    a.bmask = mask.block;
+    a.bm_per_head = mask.per_head;
+    a.nqbm = (Tq + 127) / 128;
+    a.nkbm = (Tk + 127) / 128;
+    a.masked = (mask.left >= 0 || mask.block) ? 1 : 0;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.nqb = (Tq + L::NQ * BR - 1) / (L::NQ * BR);
     a.units = BH * a.nqb;
@@ -732,25 +861,25 @@ int launch(const void *q, const void *k, const void *v, void *o, float *lse, int
     a.group = g < 1 ? 1 : (g > BH ? BH : g);
     a.timeout_ns = wait_timeout_ns();
     const int grid = a.units < device_sm_count() ? a.units : device_sm_count();
-    if (cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             L::SMEM_BYTES) != cudaSuccess)
+    auto kernel = a.masked ? fwd_kernel<D, true> : fwd_kernel<D, false>;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES) != cudaSuccess)
         return ERR_CUDA;
-    fwd_kernel<D><<<grid, L::NTHREADS, L::SMEM_BYTES, s>>>(tq, tk, tv, a);
+    kernel<<<grid, L::NTHREADS, L::SMEM_BYTES, s>>>(tq, tk, tv, a);
     return cudaGetLastError() == cudaSuccess ? OK : ERR_CUDA;
 }
 
 }  // namespace
 
 int fwd_bf16_launch(const void *q, const void *k, const void *v, void *o, float *lse, int BH, int Tq,
-                    int Tk, int d, int causal, float scale, cudaStream_t s)
+                    int Tk, int d, const MaskSpec &mask, float scale, cudaStream_t s)
 {
     switch (d) {
     case 64:
-        return launch<64>(q, k, v, o, lse, BH, Tq, Tk, causal, scale, s);
+        return launch<64>(q, k, v, o, lse, BH, Tq, Tk, mask, scale, s);
     case 128:
-        return launch<128>(q, k, v, o, lse, BH, Tq, Tk, causal, scale, s);
+        return launch<128>(q, k, v, o, lse, BH, Tq, Tk, mask, scale, s);
     case 256:
-        return launch<256>(q, k, v, o, lse, BH, Tq, Tk, causal, scale, s);
+        return launch<256>(q, k, v, o, lse, BH, Tq, Tk, mask, scale, s);
     default:
         return ERR_UNSUPPORTED;
     }

@@ -22,9 +22,21 @@ int encode_tmap_3d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype
 int device_sm_count();          // SMs of the current device (cached per device)
 uint64_t wait_timeout_ns();     // bounded-wait limit for device spin waits
 
+// Allowed (row, key) pairs: key l is allowed for row r iff
+//   r + Tk - Tq - left <= l <= r + Tk - Tq + right   (left, right = -1: that side unbounded)
+// and, with a block mask, block[(r / 128) * nkbm + l / 128] != 0 for the head's mask
+// ([heads][ceil(Tq / 128)][ceil(Tk / 128)] bytes in device memory, one mask per head when
+// per_head, else one for all heads).  Causal is left = -1, right = 0.
+struct MaskSpec {
+    int left, right;
+    const uint8_t *block;
+    int per_head;
+};
+inline MaskSpec causal_spec(int causal) { return MaskSpec{-1, causal ? 0 : -1, nullptr, 0}; }
+
 // Kernel launchers (arguments already validated by the ABI layer).
 int fwd_bf16_launch(const void *q, const void *k, const void *v, void *o, float *lse, int BH,
-                    int Tq, int Tk, int d, int causal, float scale, cudaStream_t s);
+                    int Tq, int Tk, int d, const MaskSpec &mask, float scale, cudaStream_t s);
 int fwd_f32_launch(const float *q, const float *k, const float *v, float *o, float *lse, int BH,
                    int Tq, int Tk, int d, int causal, float scale, cudaStream_t s);
 int fill_empty_launch(void *o, float *lse, size_t rows, int d, int elem_bytes, cudaStream_t s);

@@ -26,6 +26,8 @@ _lib.fa_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp
 _lib.fa_fwd.restype = _i
 _lib.fa_fwd_f32.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp]
 _lib.fa_fwd_f32.restype = _i
+_lib.fa_fwd_masked.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _i, _f, _vp]
+_lib.fa_fwd_masked.restype = _i
 _lib.fa_decode.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _sz, _vp]
 _lib.fa_decode.restype = _i
 _lib.fa_decode_workspace_bytes.argtypes = [_i, _i, _i, _i, _i]
@@ -103,6 +105,38 @@ def fa_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
     _need(lse, "lse", torch.float32, (B, H, Tq), dev)
     _check("fa_fwd", _lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Tq, Tk, d,
                                  int(bool(causal)), float(scale), _stream(stream)))
+
+
+def _block_mask(block_mask, B, H, Tq, Tk, dev):
+    """(pointer, per_head) of a block mask: a uint8/bool tensor on `dev` shaped
+    [ceil(Tq/128), ceil(Tk/128)] (all heads) or [B, H, ceil(Tq/128), ceil(Tk/128)]."""
+    if block_mask is None:
+        return None, 0
+    nq, nk = -(-Tq // 128), -(-Tk // 128)
+    if block_mask.device != dev or block_mask.dtype not in (torch.uint8, torch.bool) or \
+            not block_mask.is_contiguous():
+        raise ValueError("block_mask: contiguous uint8 or bool tensor on the inputs' device")
+    if tuple(block_mask.shape) == (nq, nk):
+        return block_mask.data_ptr(), 0
+    if tuple(block_mask.shape) == (B, H, nq, nk):
+        return block_mask.data_ptr(), 1
+    raise ValueError(f"block_mask: shape ({nq}, {nk}) or ({B}, {H}, {nq}, {nk}), got {tuple(block_mask.shape)}")
+
+
+def fa_fwd_masked(q, k, v, o, lse, window=(-1, -1), block_mask=None, scale: float = 1.0, stream=None) -> None:
+    """fa_fwd under a window (left, right) around the bottom-right diagonal (-1 = unbounded
+    side; (-1, 0) is causal) and an optional 128 x 128 block mask."""
+    B, H, Tq, Tk, d = _shapes(q, k)
+    dev = q.device
+    _need(q, "q", torch.bfloat16, (B, H, Tq, d), dev)
+    _need(k, "k", torch.bfloat16, (B, H, Tk, d), dev)
+    _need(v, "v", torch.bfloat16, (B, H, Tk, d), dev)
+    _need(o, "o", torch.bfloat16, (B, H, Tq, d), dev)
+    _need(lse, "lse", torch.float32, (B, H, Tq), dev)
+    bm, per_head = _block_mask(block_mask, B, H, Tq, Tk, dev)
+    _check("fa_fwd_masked", _lib.fa_fwd_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Tq, Tk, d,
+                                               int(window[0]), int(window[1]), bm, per_head, float(scale),
+                                               _stream(stream)))
 
 
 def fa_decode_workspace_bytes(B: int, H: int, Tq: int, Tk: int, d: int) -> int:
@@ -213,12 +247,20 @@ def fa_status_string(status: int) -> str:
 
 
 # ---------------------------------------------------------------- conveniences
-def attention_forward(q, k, v, causal: bool, scale: float, stream=None):
-    """Allocates O and lse with torch and runs fa_fwd (bf16) or fa_fwd_f32 (float32)."""
+def attention_forward(q, k, v, causal: bool, scale: float, stream=None, window=None, block_mask=None):
+    """Allocates O and lse with torch and runs fa_fwd (bf16) or fa_fwd_f32 (float32); with a
+    window (which replaces `causal`) or a block mask, fa_fwd_masked."""
     B, H, Tq, Tk, d = _shapes(q, k)
     o = torch.empty_like(q)
     lse = torch.empty((B, H, Tq), dtype=torch.float32, device=q.device)
-    (fa_fwd_f32 if q.dtype == torch.float32 else fa_fwd)(q, k, v, o, lse, causal, scale, stream)
+    if window is not None or block_mask is not None:
+        if window is None:
+            window = (-1, 0 if causal else -1)
+        elif causal:
+            raise ValueError("give either causal or a window")
+        fa_fwd_masked(q, k, v, o, lse, window, block_mask, scale, stream)
+    else:
+        (fa_fwd_f32 if q.dtype == torch.float32 else fa_fwd)(q, k, v, o, lse, causal, scale, stream)
     return o, lse
 
 

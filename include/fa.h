@@ -75,6 +75,26 @@ int fa_fwd_f32(const float *q, const float *k, const float *v, float *o, float *
                fa_stream_t stream);
 
 /*
+ * fa_fwd under a sliding window and/or a block mask (zerotofrontier.app
+ * "FlashAttention", "Dropout, block-sparsity, and other real-kernel
+ * details": windows are functions of (r, l) computed inside the tile, and
+ * tiles a block mask marks empty are skipped exactly as causal tiles are).
+ * Key l is allowed for query row r iff
+ *     r + Tk - Tq - window_left <= l <= r + Tk - Tq + window_right
+ * (-1 leaves that side unbounded: (-1, 0) is fa_fwd's causal mask, (-1, -1)
+ * no mask) and, when block_mask is not NULL, its byte for the 128 x 128 block
+ * (r / 128, l / 128) is nonzero.  block_mask is device memory, row-major
+ * [mask_per_head ? B*H : 1][ceil(Tq / 128)][ceil(Tk / 128)], read-only,
+ * owned by the caller, not overlapping o or lse.  Rows with no allowed key
+ * get O = 0 and lse = -inf.  Other arguments and errors as fa_fwd; a window
+ * side below -1 or mask_per_head outside {0, 1} is FA_ERR_INVALID_ARG.
+ */
+int fa_fwd_masked(const void *q, const void *k, const void *v, void *o, float *lse,
+                  int B, int H, int Tq, int Tk, int d, int window_left, int window_right,
+                  const unsigned char *block_mask, int mask_per_head, float scale,
+                  fa_stream_t stream);
+
+/*
  * Split-KV attention for decoding: the O and lse of fa_fwd for a few query
  * rows per head against a long key/value sequence (atlas.blal.pro
  * "FlashAttention -- IO-Aware Exact Attention", "Honest caveats & open
