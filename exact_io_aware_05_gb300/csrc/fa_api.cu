@@ -299,12 +299,14 @@ size_t fa_bwd_workspace_bytes(int B, int H, int Tq, int Tk, int d)
 }
 
 static int bwd_common(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dO,
-                      void *dq, void *dk, void *dv, int B, int H, int Tq, int Tk, int d, int causal, float scale,
-                      void *workspace, size_t workspace_bytes, int stages, fa_stream_t stream)
+                      void *dq, void *dk, void *dv, int B, int H, int Tq, int Tk, int d, const fa::MaskSpec &mask,
+                      float scale, void *workspace, size_t workspace_bytes, int stages, fa_stream_t stream)
 {
-    int st = fa::check_sizes(B, H, Tq, Tk, d, causal, scale);
+    int st = fa::check_sizes(B, H, Tq, Tk, d, 0, scale);
     if (st != fa::OK)
         return st;
+    if (mask.left < -1 || mask.right < -1 || mask.per_head < 0 || mask.per_head > 1)
+        return FA_ERR_INVALID_ARG;
     if (d == 256)
         return FA_ERR_UNSUPPORTED;
     const size_t bh = (size_t)B * H;
@@ -330,39 +332,62 @@ static int bwd_common(const void *q, const void *k, const void *v, const void *o
         for (int j = i + 1; j < 4; ++j)
             if (fa::overlaps(outs[i], out_n[i], outs[j], out_n[j]))
                 return FA_ERR_INVALID_ARG;
+        if (mask.block) {
+            const size_t nm = (mask.per_head ? bh : 1) * (size_t)((Tq + 127) / 128) * ((Tk + 127) / 128);
+            if (fa::overlaps(outs[i], out_n[i], mask.block, nm))
+                return FA_ERR_INVALID_ARG;
+        }
     }
     st = fa::check_device();
     if (st != fa::OK)
         return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const fa::BwdWorkspace ws = fa::bwd_workspace_carve(workspace, (int)bh, Tq, d);
-    return fa::bwd_launch(q, k, v, o, lse, dO, dq, dk, dv, (int)bh, Tq, Tk, d, causal, scale, ws, stages, s);
+    return fa::bwd_launch(q, k, v, o, lse, dO, dq, dk, dv, (int)bh, Tq, Tk, d, mask, scale, ws, stages, s);
 }
+
+static int causal_ok(int causal) { return causal == 0 || causal == 1; }
 
 int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dO, void *dq,
            void *dk, void *dv, int B, int H, int Tq, int Tk, int d, int causal, float scale, void *workspace,
            size_t workspace_bytes, fa_stream_t stream)
 {
-    return bwd_common(q, k, v, o, lse, dO, dq, dk, dv, B, H, Tq, Tk, d, causal, scale, workspace, workspace_bytes, 7,
-                      stream);
+    if (!causal_ok(causal))
+        return FA_ERR_INVALID_ARG;
+    return bwd_common(q, k, v, o, lse, dO, dq, dk, dv, B, H, Tq, Tk, d, fa::causal_spec(causal), scale, workspace,
+                      workspace_bytes, 7, stream);
+}
+
+int fa_bwd_masked(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dO,
+                  void *dq, void *dk, void *dv, int B, int H, int Tq, int Tk, int d, int window_left, int window_right,
+                  const unsigned char *block_mask, int mask_per_head, int deterministic, float scale,
+                  void *workspace, size_t workspace_bytes, fa_stream_t stream)
+{
+    if (deterministic < 0 || deterministic > 1)
+        return FA_ERR_INVALID_ARG;
+    const fa::MaskSpec m{window_left, window_right, block_mask, mask_per_head};
+    return bwd_common(q, k, v, o, lse, dO, dq, dk, dv, B, H, Tq, Tk, d, m, scale, workspace, workspace_bytes,
+                      7 | (deterministic ? fa::kBwdDeterministic : 0), stream);
 }
 
 int fa_bwd_deterministic(const void *q, const void *k, const void *v, const void *o, const float *lse,
                          const void *dO, void *dq, void *dk, void *dv, int B, int H, int Tq, int Tk, int d,
                          int causal, float scale, void *workspace, size_t workspace_bytes, fa_stream_t stream)
 {
-    return bwd_common(q, k, v, o, lse, dO, dq, dk, dv, B, H, Tq, Tk, d, causal, scale, workspace, workspace_bytes,
-                      7 | fa::kBwdDeterministic, stream);
+    if (!causal_ok(causal))
+        return FA_ERR_INVALID_ARG;
+    return bwd_common(q, k, v, o, lse, dO, dq, dk, dv, B, H, Tq, Tk, d, fa::causal_spec(causal), scale, workspace,
+                      workspace_bytes, 7 | fa::kBwdDeterministic, stream);
 }
 
 int fa_bwd_stage(int stage, const void *q, const void *k, const void *v, const void *o, const float *lse,
                  const void *dO, void *dq, void *dk, void *dv, int B, int H, int Tq, int Tk, int d, int causal,
                  float scale, void *workspace, size_t workspace_bytes, fa_stream_t stream)
 {
-    if (stage < 1 || stage > 3)
+    if (stage < 1 || stage > 3 || !causal_ok(causal))
         return FA_ERR_INVALID_ARG;
-    return bwd_common(q, k, v, o, lse, dO, dq, dk, dv, B, H, Tq, Tk, d, causal, scale, workspace, workspace_bytes,
-                      1 << (stage - 1), stream);
+    return bwd_common(q, k, v, o, lse, dO, dq, dk, dv, B, H, Tq, Tk, d, fa::causal_spec(causal), scale, workspace,
+                      workspace_bytes, 1 << (stage - 1), stream);
 }
 
 int fa_sync_status(fa_stream_t stream)

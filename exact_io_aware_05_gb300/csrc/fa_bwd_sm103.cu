@@ -101,6 +101,11 @@ struct BwdArgs {
     int nkb, units, group;
     uint64_t timeout_ns;
     const int *det_bound;   // deterministic mode: per 128-row query block, bound on |dq_acc| (else null)
+    // masked instance: allowed keys of row r are r + Tk - Tq - left .. r + Tk - Tq + right
+    // (-1: unbounded side), in 128 x 128 blocks marked by bmask ([heads][nqbm][nkbm] or null)
+    int left, right;
+    const uint8_t *bmask;
+    int bm_per_head, nqbm, nkbm;
 };
 
 // Deterministic mode.  dQ_i is a sum over key blocks whose terms arrive in any
@@ -122,9 +127,21 @@ __device__ __forceinline__ float det_block_scale(int bound_bits)
 
 struct Unit {
     int bh, j;     // head, key block
-    int i0, nq;    // first query block, number of query blocks
+    int i0, nq;    // first query block, number of query blocks visited
+    int i1;        // last query block visited
+    const uint8_t *bm;   // masked instance: the key block's mask column (stride nkbm), or null
 };
 
+// The first query block at or after i that unit x visits (i1 + 1 if none).
+__device__ __forceinline__ int unit_next(const Unit &x, int i, int nkbm)
+{
+    while (i <= x.i1 && x.bm && !x.bm[(size_t)i * nkbm])
+        ++i;
+    return i;
+}
+
+// MASKED = false: causal or not, every unit visits a contiguous run of query blocks.
+template <bool MASKED>
 __device__ __forceinline__ Unit make_unit(int u, const BwdArgs &a)
 {
     const int per_group = a.group * a.nkb;
@@ -145,6 +162,37 @@ __device__ __forceinline__ Unit make_unit(int u, const BwdArgs &a)
     x.nq = nqb - x.i0;
     if (x.nq < 0)
         x.nq = 0;
+    x.i1 = x.i0 + x.nq - 1;
+    x.bm = nullptr;
+    if constexpr (MASKED) {
+        // rows that see some key of the block: r >= first key - off - right (right bound),
+        // r <= last key - off + left (left bound); then the block mask's column
+        const long off = (long)a.Tk - a.Tq;
+        const long kf = (long)x.j * BK, kl = min((long)a.Tk - 1, kf + BK - 1);
+        const long rlo = a.right >= 0 ? max(0L, kf - off - a.right) : 0L;
+        const long rhi = a.left >= 0 ? min((long)a.Tq - 1, kl - off + a.left) : (long)a.Tq - 1;
+        if (rlo > rhi) {
+            x.nq = 0;
+            x.i1 = x.i0 - 1;
+            return x;
+        }
+        x.i0 = (int)(rlo / BQ);
+        x.i1 = (int)(rhi / BQ);
+        if (a.bmask) {
+            x.bm = a.bmask + (size_t)(a.bm_per_head ? x.bh : 0) * a.nqbm * a.nkbm + x.j;
+            // count with i1 still the window's last block; then narrow it to the last marked one
+            int n = 0, last = x.i0 - 1;
+            x.i0 = unit_next(x, x.i0, a.nkbm);
+            for (int i = x.i0; i <= x.i1; i = unit_next(x, i + 1, a.nkbm)) {
+                ++n;
+                last = i;
+            }
+            x.nq = n;
+            x.i1 = last;
+        } else {
+            x.nq = x.i1 - x.i0 + 1;
+        }
+    }
     return x;
 }
 
@@ -166,7 +214,8 @@ __device__ __forceinline__ uint32_t half_packed_col(int kk) { return (kk >> 2) *
 
 // P = exp2(c log2(e) S - lse log2(e)) for 32 query columns of one key row, in place.
 template <bool MASK>
-__device__ __forceinline__ void softmax_p32(uint32_t (&sv)[32], const float4 *nl4, float sl2, int q0, int qmin)
+__device__ __forceinline__ void softmax_p32(uint32_t (&sv)[32], const float4 *nl4, float sl2, int q0, int qmin,
+                                            int qmax)
 {
 #pragma unroll
     for (int e4 = 0; e4 < 8; ++e4) {
@@ -180,10 +229,10 @@ __device__ __forceinline__ void softmax_p32(uint32_t (&sv)[32], const float4 *nl
         p3 = ex2_approx(p3);
         if (MASK) {
             const int q = q0 + 4 * e4;
-            p0 = q >= qmin ? p0 : 0.f;
-            p1 = q + 1 >= qmin ? p1 : 0.f;
-            p2 = q + 2 >= qmin ? p2 : 0.f;
-            p3 = q + 3 >= qmin ? p3 : 0.f;
+            p0 = (q >= qmin && q < qmax) ? p0 : 0.f;
+            p1 = (q + 1 >= qmin && q + 1 < qmax) ? p1 : 0.f;
+            p2 = (q + 2 >= qmin && q + 2 < qmax) ? p2 : 0.f;
+            p3 = (q + 3 >= qmin && q + 3 < qmax) ? p3 : 0.f;
         }
         sv[4 * e4] = __float_as_uint(p0);
         sv[4 * e4 + 1] = __float_as_uint(p1);
@@ -192,7 +241,7 @@ __device__ __forceinline__ void softmax_p32(uint32_t (&sv)[32], const float4 *nl
     }
 }
 
-template <int D>
+template <int D, bool MASKED>
 __global__ void __launch_bounds__(512, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -260,7 +309,7 @@ __global__ void __launch_bounds__(512, 1)
             uint32_t n_kv = 0, n_st = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
-                const Unit x = make_unit(u, a);
+                const Unit x = make_unit<MASKED>(u, a);
                 if (x.nq == 0)
                     continue;
                 if (n_kv > 0 && !mbar_wait<true>(bar(L::B_KVEMPTY), (n_kv - 1) & 1, ctx, SITE_P_KVEMPTY))
@@ -271,7 +320,7 @@ __global__ void __launch_bounds__(512, 1)
                     tma_load_3d(sbase + L::OFF_V + c * L::KV_CHUNK, &tm_v, bar(L::B_KVFULL), c * 64, x.j * BK, x.bh);
                 }
                 ++n_kv;
-                for (int i = x.i0; i < x.i0 + x.nq; ++i) {
+                for (int k = 0, i = x.i0; k < x.nq; ++k, i = MASKED ? unit_next(x, i + 1, a.nkbm) : i + 1) {
                     const uint32_t s = n_st % NST;
                     if (n_st >= NST && !mbar_wait<true>(bar(L::B_STEMPTY + s), ((n_st / NST) - 1) & 1, ctx, SITE_P_STEMPTY)) {
                         ok = false;
@@ -327,7 +376,7 @@ __global__ void __launch_bounds__(512, 1)
                 return true;
             };
             for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
-                const Unit x = make_unit(u, a);
+                const Unit x = make_unit<MASKED>(u, a);
                 if (x.nq == 0)
                     continue;
                 if (!mbar_wait<true>(bar(L::B_KVFULL), nu & 1, ctx, SITE_M_KVFULL) || !issue_s(g))
@@ -427,9 +476,9 @@ __global__ void __launch_bounds__(512, 1)
             uint32_t g = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
-                const Unit x = make_unit(u, a);
-                for (int i = 0; i < x.nq; ++i, ++g) {
-                    const size_t roff = (size_t)x.bh * a.Tq_pad + (size_t)(x.i0 + i) * BQ;
+                const Unit x = make_unit<MASKED>(u, a);
+                for (int i = 0, qi = x.i0; i < x.nq; ++i, ++g, qi = MASKED ? unit_next(x, qi + 1, a.nkbm) : qi + 1) {
+                    const size_t roff = (size_t)x.bh * a.Tq_pad + (size_t)qi * BQ;
                     if (g > 0 && !mbar_wait<true>(bar(L::B_PFULL), (g - 1) & 1, ctx, SITE_L_PFULL)) {
                         ok = false;
                         break;
@@ -461,17 +510,24 @@ __global__ void __launch_bounds__(512, 1)
         uint32_t g = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
-            const Unit x = make_unit(u, a);
+            const Unit x = make_unit<MASKED>(u, a);
             const int l = x.j * BK + key_in_blk;         // this thread's key
-            for (int i = 0; i < x.nq; ++i, ++g) {
-                const int qb = (x.i0 + i) * BQ + half * 64;        // first query row of this half
+            for (int i = 0, qi = x.i0; i < x.nq; ++i, ++g, qi = MASKED ? unit_next(x, qi + 1, a.nkbm) : qi + 1) {
+                const int qb = qi * BQ + half * 64;   // first query row of this half
                 // column q is allowed iff the key exists and (causal) qb + q >= l - (Tk - Tq)
-                int qmin = l < a.Tk ? 0 : 64;
+                int qmin = l < a.Tk ? 0 : 64, qmax = 64;   // allowed query columns [qmin, qmax)
                 if (a.causal && l < a.Tk) {
                     const long lim = (long)l - (a.Tk - a.Tq) - qb;
                     qmin = (int)max(0L, min(64L, lim));
                 }
-                const bool mask = __any_sync(0xffffffffu, qmin > 0);
+                if (MASKED && l < a.Tk) {
+                    const long off = (long)a.Tk - a.Tq;
+                    if (a.right >= 0)
+                        qmin = (int)max(0L, min(64L, (long)l - off - a.right - qb));
+                    if (a.left >= 0)
+                        qmax = (int)max(0L, min(64L, (long)l - off + a.left - qb + 1));
+                }
+                const bool mask = __any_sync(0xffffffffu, qmin > 0 || qmax < 64);
                 if (!mbar_wait(bar(L::B_SFULL), g & 1, ctx, SITE_S_SFULL) ||
                     !mbar_wait(bar(L::B_LFULL), g & 1, ctx, SITE_S_LFULL)) {
                     ok = false;
@@ -486,11 +542,11 @@ __global__ void __launch_bounds__(512, 1)
                 tmem_wait_ld_x32(p1);
                 const float4 *nl4 = reinterpret_cast<const float4 *>(smem + L::OFF_LSE) + half * 16;
                 if (mask) {
-                    softmax_p32<true>(p0, nl4, sl2, 0, qmin);
-                    softmax_p32<true>(p1, nl4 + 8, sl2, 32, qmin);
+                    softmax_p32<true>(p0, nl4, sl2, 0, qmin, qmax);
+                    softmax_p32<true>(p1, nl4 + 8, sl2, 32, qmin, qmax);
                 } else {
-                    softmax_p32<false>(p0, nl4, sl2, 0, 0);
-                    softmax_p32<false>(p1, nl4 + 8, sl2, 32, 0);
+                    softmax_p32<false>(p0, nl4, sl2, 0, 0, 64);
+                    softmax_p32<false>(p1, nl4 + 8, sl2, 32, 0, 64);
                 }
                 {
                     uint32_t pk[16];
@@ -555,7 +611,7 @@ __global__ void __launch_bounds__(512, 1)
         uint32_t g = 0, nu = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
-            const Unit x = make_unit(u, a);
+            const Unit x = make_unit<MASKED>(u, a);
             const int l = x.j * BK + row;
             const size_t krow = (size_t)x.bh * a.Tk + l;
             if (x.nq == 0) {
@@ -569,7 +625,7 @@ __global__ void __launch_bounds__(512, 1)
                 }
                 continue;
             }
-            for (int i = 0; i < x.nq; ++i, ++g) {
+            for (int i = 0, qi = x.i0; i < x.nq; ++i, ++g, qi = MASKED ? unit_next(x, qi + 1, a.nkbm) : qi + 1) {
                 const uint32_t b = L::DQ_ALIAS ? 0u : (g & 1u);
                 const uint32_t ph = L::DQ_ALIAS ? (g & 1u) : ((g >> 1) & 1u);
                 if (!mbar_wait<true>(bar(L::B_DQFULL + b), ph, ctx, SITE_D_DQFULL)) {
@@ -577,7 +633,7 @@ __global__ void __launch_bounds__(512, 1)
                     break;
                 }
                 tc_fence_after();
-                const int qb = (x.i0 + i) * BQ;
+                const int qb = qi * BQ;
                 float *acc = a.dq_acc + ((size_t)x.bh * a.Tq_pad + qb) * D;
                 const float dsc = a.det_bound ? det_block_scale(a.det_bound[((size_t)x.bh * a.Tq_pad + qb) / BQ]) : 0.f;
                 int *iacc = reinterpret_cast<int *>(acc);
@@ -819,9 +875,11 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float *__restrict__ d
 
 template <int D>
 int launch_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dO,
-               void *dq, void *dk, void *dv, int BH, int Tq, int Tk, int causal, float scale,
+               void *dq, void *dk, void *dv, int BH, int Tq, int Tk, const MaskSpec &mask, float scale,
                const BwdWorkspace &ws, int stages, cudaStream_t s)
 {
+    const int causal = mask.right == 0 ? 1 : 0;
+    const bool masked = mask.left >= 0 || mask.right > 0 || mask.block;
     using L = BwdLayout<D>;
     const int Tq_pad = (int)bwd_row_stride(Tq);
     const int sms = device_sm_count();
@@ -883,11 +941,17 @@ int launch_bwd(const void *q, const void *k, const void *v, const void *o, const
         a.group = gsz < 1 ? 1 : (gsz > BH ? BH : gsz);
         a.timeout_ns = wait_timeout_ns();
         a.det_bound = det ? ws.bound : nullptr;
-        if (cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES) !=
-            cudaSuccess)
+        a.left = mask.left;
+        a.right = mask.right;
+        a.bmask = mask.block;
+        a.bm_per_head = mask.per_head;
+        a.nqbm = (Tq + 127) / 128;
+        a.nkbm = (Tk + 127) / 128;
+        auto kernel = masked ? bwd_main_kernel<D, true> : bwd_main_kernel<D, false>;
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES) != cudaSuccess)
             return ERR_CUDA;
         const int grid = a.units < sms ? a.units : sms;
-        bwd_main_kernel<D><<<grid, L::NTHREADS, L::SMEM_BYTES, s>>>(tq, tk, tv, tdo, a);
+        kernel<<<grid, L::NTHREADS, L::SMEM_BYTES, s>>>(tq, tk, tv, tdo, a);
         if (cudaGetLastError() != cudaSuccess)
             return ERR_CUDA;
     }
@@ -907,14 +971,14 @@ int launch_bwd(const void *q, const void *k, const void *v, const void *o, const
 }  // namespace
 
 int bwd_launch(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dO, void *dq,
-               void *dk, void *dv, int BH, int Tq, int Tk, int d, int causal, float scale, const BwdWorkspace &ws,
-               int stages, cudaStream_t s)
+               void *dk, void *dv, int BH, int Tq, int Tk, int d, const MaskSpec &mask, float scale,
+               const BwdWorkspace &ws, int stages, cudaStream_t s)
 {
     switch (d) {
     case 64:
-        return launch_bwd<64>(q, k, v, o, lse, dO, dq, dk, dv, BH, Tq, Tk, causal, scale, ws, stages, s);
+        return launch_bwd<64>(q, k, v, o, lse, dO, dq, dk, dv, BH, Tq, Tk, mask, scale, ws, stages, s);
     case 128:
-        return launch_bwd<128>(q, k, v, o, lse, dO, dq, dk, dv, BH, Tq, Tk, causal, scale, ws, stages, s);
+        return launch_bwd<128>(q, k, v, o, lse, dO, dq, dk, dv, BH, Tq, Tk, mask, scale, ws, stages, s);
     default:
         return ERR_UNSUPPORTED;
     }

@@ -60,7 +60,7 @@ BwdWorkspace bwd_workspace_carve(void *ws, int BH, int Tq, int d);
 constexpr int kBwdDeterministic = 8;
 int bwd_launch(const void *q, const void *k, const void *v, const void *o, const float *lse,
                const void *dO, void *dq, void *dk, void *dv, int BH, int Tq, int Tk, int d,
-               int causal, float scale, const BwdWorkspace &ws, int stages, cudaStream_t s);
+               const MaskSpec &mask, float scale, const BwdWorkspace &ws, int stages, cudaStream_t s);
 
 // Split-KV decode (fa_decode_sm103.cu): chunks per head and key tiles per
 // chunk for these sizes, partial-state workspace bytes, query rows allowed per

@@ -28,6 +28,8 @@ _lib.fa_fwd_f32.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f,
 _lib.fa_fwd_f32.restype = _i
 _lib.fa_fwd_masked.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _i, _f, _vp]
 _lib.fa_fwd_masked.restype = _i
+_lib.fa_bwd_masked.argtypes = [_vp] * 9 + [_i] * 7 + [_vp, _i, _i, _f, _vp, _sz, _vp]
+_lib.fa_bwd_masked.restype = _i
 _lib.fa_decode.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _sz, _vp]
 _lib.fa_decode.restype = _i
 _lib.fa_decode_workspace_bytes.argtypes = [_i, _i, _i, _i, _i]
@@ -269,12 +271,41 @@ def alloc_workspace(B, H, Tq, Tk, d, device) -> torch.Tensor:
     return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
 
 
+def fa_bwd_masked(q, k, v, o, lse, dO, dq, dk, dv, window=(-1, -1), block_mask=None, deterministic=False,
+                  scale: float = 1.0, workspace: torch.Tensor = None, stream=None) -> None:
+    """Backward of fa_fwd_masked under the same window and block mask."""
+    B, H, Tq, Tk, d = _shapes(q, k)
+    dev = q.device
+    for name, t, shp in (("q", q, (B, H, Tq, d)), ("k", k, (B, H, Tk, d)), ("v", v, (B, H, Tk, d)),
+                         ("o", o, (B, H, Tq, d)), ("dO", dO, (B, H, Tq, d)), ("dq", dq, (B, H, Tq, d)),
+                         ("dk", dk, (B, H, Tk, d)), ("dv", dv, (B, H, Tk, d))):
+        _need(t, name, torch.bfloat16, shp, dev)
+    _need(lse, "lse", torch.float32, (B, H, Tq), dev)
+    if workspace is None or workspace.device != dev or not workspace.is_contiguous():
+        raise ValueError("workspace: a contiguous tensor on the same device")
+    bm, per_head = _block_mask(block_mask, B, H, Tq, Tk, dev)
+    nbytes = workspace.numel() * workspace.element_size()
+    _check("fa_bwd_masked", _lib.fa_bwd_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
+                                               _ptr(dk), _ptr(dv), B, H, Tq, Tk, d, int(window[0]), int(window[1]),
+                                               bm, per_head, int(bool(deterministic)), float(scale),
+                                               _ptr(workspace), nbytes, _stream(stream)))
+
+
 def attention_backward(q, k, v, o, lse, dO, causal: bool, scale: float, workspace=None, stream=None,
-                       deterministic: bool = False):
+                       deterministic: bool = False, window=None, block_mask=None):
     """Allocates dQ, dK, dV (and the workspace if not given) and runs fa_bwd
-    (fa_bwd_deterministic when `deterministic`)."""
+    (fa_bwd_deterministic when `deterministic`; fa_bwd_masked with a window, which
+    replaces `causal`, or a block mask)."""
     B, H, Tq, Tk, d = _shapes(q, k)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws = alloc_workspace(B, H, Tq, Tk, d, q.device) if workspace is None else workspace
-    (fa_bwd_deterministic if deterministic else fa_bwd)(q, k, v, o, lse, dO, dq, dk, dv, causal, scale, ws, stream)
+    if window is not None or block_mask is not None:
+        if window is None:
+            window = (-1, 0 if causal else -1)
+        elif causal:
+            raise ValueError("give either causal or a window")
+        fa_bwd_masked(q, k, v, o, lse, dO, dq, dk, dv, window, block_mask, deterministic, scale, ws, stream)
+    else:
+        (fa_bwd_deterministic if deterministic else fa_bwd)(q, k, v, o, lse, dO, dq, dk, dv, causal, scale, ws,
+                                                            stream)
     return dq, dk, dv

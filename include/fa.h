@@ -159,6 +159,21 @@ int fa_bwd_deterministic(const void *q, const void *k, const void *v, const void
                          void *workspace, size_t workspace_bytes, fa_stream_t stream);
 
 /*
+ * Backward of fa_fwd_masked: the gradients under the same window and block
+ * mask (see fa_fwd_masked for their meaning, layout and ownership; o and lse
+ * must come from fa_fwd_masked with the same mask).  Each 128-key block
+ * visits only the query blocks that its window and mask admit.
+ * deterministic = 1 selects fa_bwd_deterministic's order-independent dQ.
+ * Other arguments, workspace and errors as fa_bwd; window sides below -1,
+ * mask_per_head or deterministic outside {0, 1} are FA_ERR_INVALID_ARG.
+ */
+int fa_bwd_masked(const void *q, const void *k, const void *v, const void *o,
+                  const float *lse, const void *dO, void *dq, void *dk, void *dv,
+                  int B, int H, int Tq, int Tk, int d, int window_left, int window_right,
+                  const unsigned char *block_mask, int mask_per_head, int deterministic,
+                  float scale, void *workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/*
  * One stage of fa_bwd, for callers that schedule or time the three kernels
  * separately: stage 1 computes D_r = dO_r . O_r and the log2-domain lse into
  * the workspace and zeroes the dQ accumulator; stage 2 runs the tile loop

@@ -10,7 +10,7 @@ import torch
 
 import oracle
 from exact_io_aware_05_gb300 import inputs
-from gpu_util import TOL_LSE, TOL_O_BF16, fwd_errors, heads_of, rows_of, to64
+from gpu_util import TOL_GRAD, TOL_LSE, TOL_O_BF16, fwd_errors, half_ulp_bf16, heads_of, rows_of, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -97,3 +97,59 @@ def test_masked_errors(fa):
     with pytest.raises(ValueError):
         fa.fa_fwd_masked(q, q, q, o, lse, (-1, 0), torch.ones(2, 2, dtype=torch.uint8, device="cuda"), 0.1)
     assert fa.fa_sync_status() == fa.FA_OK
+
+
+# ---------------------------------------------------------------- backward under masks
+GUARD = 1 << 20
+def check_bwd(fa, w, window, bmask, heads, deterministic=False):
+    x = inputs.generate(w, with_grad=True, device="cuda")
+    bm_dev = None if bmask is None else bmask.to("cuda")
+    o, lse = fa.attention_forward(x["q"], x["k"], x["v"], False, w.scale, window=window, block_mask=bm_dev)
+    # a guard band after the workspace: the kernels must leave it untouched
+    need = fa.fa_bwd_workspace_bytes(w.B, w.H, w.Tq, w.Tk, w.d)
+    ws = torch.full((need + GUARD,), 0xA5, dtype=torch.uint8, device="cuda")
+    dq, dk, dv = fa.attention_backward(x["q"], x["k"], x["v"], o, lse, x["do"], False, w.scale, workspace=ws[:need],
+                                       window=window, block_mask=bm_dev, deterministic=deterministic)
+    assert fa.fa_sync_status() == fa.FA_OK
+    assert bool(torch.all(ws[need:] == 0xA5)), "write past the end of the workspace"
+    worst = {"dq": 0.0, "dk": 0.0, "dv": 0.0}
+    for (b, h) in heads:
+        q, k, v, do = (to64(x[n][b, h]) for n in ("q", "k", "v", "do"))
+        hm = None if bmask is None else (bmask.numpy() if bmask.dim() == 2 else bmask[b, h].numpy())
+        ref = oracle.attention_bwd(q, k, v, do, False, w.scale, window=window, block_mask=hm)
+        for n, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+            g = to64(t[b, h])
+            assert np.all(np.isfinite(g)), n
+            worst[n] = max(worst[n], float((np.abs(g - ref[n]) - half_ulp_bf16(ref[n])).max()))
+    print(f"{w.name} bwd window={window} mask={'none' if bmask is None else tuple(bmask.shape)} "
+          f"det={deterministic}: beyond bf16 rounding " + " ".join(f"{n}={v:.3e}" for n, v in worst.items()))
+    for n, v in worst.items():
+        assert v <= TOL_GRAD, (n, worst)
+    return dq, dk, dv
+
+
+BWD_SHAPES = [(1, 2, 700, 700, 128), (1, 2, 300, 900, 64), (1, 2, 900, 300, 128), (2, 1, 520, 520, 64)]
+
+
+@pytest.mark.parametrize("B,H,Tq,Tk,d", BWD_SHAPES)
+@pytest.mark.parametrize("window", [(127, 0), (0, 0), (64, 64), (-1, 5), (200, -1)])
+def test_bwd_windows(fa, B, H, Tq, Tk, d, window):
+    w = inputs.small(B, H, Tq, Tk, d, False, seed=Tq + 3 * Tk + d + window[0], backward=True)
+    check_bwd(fa, w, window, None, heads_of(w, B * H))
+
+
+@pytest.mark.parametrize("B,H,Tq,Tk,d", BWD_SHAPES)
+@pytest.mark.parametrize("per_head", [False, True])
+def test_bwd_block_masks(fa, B, H, Tq, Tk, d, per_head):
+    w = inputs.small(B, H, Tq, Tk, d, False, seed=Tq + 5 * Tk + d, backward=True)
+    bm = random_mask(B, H, Tq, Tk, per_head, seed=Tq + Tk + d)
+    check_bwd(fa, w, (-1, -1), bm, heads_of(w, B * H))
+    check_bwd(fa, w, (150, 10), bm, heads_of(w, B * H))
+
+
+def test_bwd_masked_deterministic(fa):
+    w = inputs.small(1, 2, 700, 700, 128, False, seed=21, backward=True)
+    bm = random_mask(1, 2, 700, 700, True, seed=22)
+    a = check_bwd(fa, w, (300, 0), bm, heads_of(w, 2), deterministic=True)
+    b = check_bwd(fa, w, (300, 0), bm, heads_of(w, 2), deterministic=True)
+    assert all(torch.equal(s.view(torch.int16), t.view(torch.int16)) for s, t in zip(a, b))
