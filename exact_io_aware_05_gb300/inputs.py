@@ -83,6 +83,10 @@ WORKLOADS = {
     # (bottom-right causal: the new row sees the whole cache), and 4 rows at 128K keys
     "decode_b8h32_q1_k32768_d128": Workload("decode_b8h32_q1_k32768_d128", 8, 32, 1, 32768, 128, True,
                                             1.0 / 128 ** 0.5, torch.bfloat16, seed=6),
+    # FP8 forward (quantized inside the path) on the 4096/d128 shape, the same inputs as the
+    # bf16 forward of that shape
+    "fwd_fp8_b8h32_t4096_d128_causal": Workload("fwd_fp8_b8h32_t4096_d128_causal", 8, 32, 4096, 4096, 128,
+                                                True, 1.0 / math.sqrt(128), torch.bfloat16, seed=1),
     "decode_b1h32_q4_k131072_d128": Workload("decode_b1h32_q4_k131072_d128", 1, 32, 4, 131072, 128, True,
                                              1.0 / 128 ** 0.5, torch.bfloat16, seed=7),
 }
@@ -113,4 +117,12 @@ def generate(w: Workload, with_grad: bool | None = None, device: str = "cpu"):
     return out
 
 
-__all__ = ["Workload", "WORKLOADS", "allowed_pairs", "generate", "small", "replace"]
+def rotation_signs(d: int, seed: int) -> torch.Tensor:
+    """The FP8 forward's random rotation signs: d values +1.0 / -1.0 (fp32), each drawn
+    as a fair bit by a torch.Generator seeded with `seed`."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    return torch.randint(0, 2, (d,), generator=g).to(torch.float32) * 2.0 - 1.0
+
+
+__all__ = ["Workload", "WORKLOADS", "allowed_pairs", "generate", "rotation_signs", "small", "replace"]

@@ -9,7 +9,8 @@ with that path.
 its analytic gradient, in double precision, one head at a time); this module
 only compiles it with the host C compiler, marshals numpy arrays and picks the
 thread count.  ``tiled.py`` holds a test-only fp64 model of the tiled
-algorithm and its memory-traffic counters.
+algorithm and its memory-traffic counters; ``fp8.py`` the FP8 forward's
+quantization (numpy) on top of the fp64 attention here.
 """
 from __future__ import annotations
 
