@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 SO = os.path.join(PKG, "libfa.so")
 SOURCES = ["fa_api.cu", "fa_fwd_sm103.cu", "fa_fwd_f32.cu", "fa_bwd_sm103.cu", "fa_bwd_noalloc.cu",
-           "fa_decode_sm103.cu"]
+           "fa_decode_sm103.cu", "fa_fp8_sm103.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -41,11 +41,20 @@ constexpr int kMaxDevices = 64;
 int encode_tmap_3d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes, uint64_t inner,
                    uint64_t rows, uint64_t planes, uint32_t box_inner, uint32_t box_rows)
 {
+    return encode_tmap_3d_strided(map, base, dtype, elem_bytes, inner, rows, planes, inner * (uint64_t)elem_bytes,
+                                  box_inner, box_rows);
+}
+
+int encode_tmap_3d_strided(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes,
+                           uint64_t inner, uint64_t rows, uint64_t planes, uint64_t row_stride, uint32_t box_inner,
+                           uint32_t box_rows)
+{
     EncodeTiledFn fn = encode_fn();
     if (!fn)
         return ERR_CUDA;
+    (void)elem_bytes;
     const cuuint64_t dims[3] = {inner, rows, planes};
-    const cuuint64_t strides[2] = {inner * (uint64_t)elem_bytes, rows * inner * (uint64_t)elem_bytes};
+    const cuuint64_t strides[2] = {row_stride, rows * row_stride};
     const cuuint32_t box[3] = {box_inner, box_rows, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     const CUresult r = fn(map, dtype, 3, const_cast<void *>(base), dims, strides, box, estr,
@@ -103,6 +112,9 @@ int fill_empty_launch(void *o, float *lse, size_t rows, int d, int elem_bytes, c
 namespace {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// A buffer of n elements: non-null and 16-byte aligned, or anything when n == 0.
+bool present16(const void *p, size_t n) { return n == 0 || (p && aligned16(p)); }
 
 bool overlaps(const void *a, size_t na, const void *b, size_t nb)
 {
@@ -239,6 +251,79 @@ int fa_fwd_masked(const void *q, const void *k, const void *v, void *o, float *l
         return fa::fill_empty_launch(o, lse, (size_t)BH * Tq, d, 2, s);
     const fa::MaskSpec m{window_left, window_right, block_mask, mask_per_head};
     return fa::fwd_bf16_launch(q, k, v, o, lse, BH, Tq, Tk, d, m, scale, s);
+}
+
+size_t fa_fp8_vt_stride(int Tk) { return Tk < 0 ? 0 : fa::fp8_vt_stride(Tk); }
+
+int fa_fp8_quantize(const void *q, const void *k, const void *v, const float *signs, int B, int H, int Tq, int Tk,
+                    int d, void *q8, void *k8, void *vt8, float *q_descale, float *k_descale, float *v_descale,
+                    fa_stream_t stream)
+{
+    int st = fa::check_sizes(B, H, Tq, Tk, d, 0, 1.f);
+    if (st != fa::OK)
+        return st;
+    const int BH = B * H;
+    const size_t nq = (size_t)BH * Tq * d, nk = (size_t)BH * Tk * d, nvt = (size_t)BH * d * fa::fp8_vt_stride(Tk);
+    // buffers of a tensor with no elements may be null
+    if (!fa::present16(q, nq) || !fa::present16(q8, nq) || !fa::present16(q_descale, nq) ||
+        !fa::present16(k, nk) || !fa::present16(v, nk) || !fa::present16(k8, nk) || !fa::present16(vt8, nk) ||
+        !fa::present16(k_descale, nk) || !fa::present16(v_descale, nk) || (signs && !fa::aligned16(signs)))
+        return FA_ERR_INVALID_ARG;
+    const size_t nqd = (size_t)BH * ((Tq + 127) / 128) * 4, nkd = (size_t)BH * ((Tk + 127) / 128) * 4,
+                 nvd = (size_t)BH * d * 4;
+    const void *outs[6] = {q8, k8, vt8, q_descale, k_descale, v_descale};
+    const size_t nouts[6] = {nq, nk, nvt, nqd, nkd, nvd};
+    const void *ins[4] = {q, k, v, signs};
+    const size_t nins[4] = {nq * 2, nk * 2, nk * 2, signs ? (size_t)d * 4 : 0};
+    for (int i = 0; i < 6; ++i) {
+        for (int j = 0; j < 4; ++j)
+            if (fa::overlaps(outs[i], nouts[i], ins[j], nins[j]))
+                return FA_ERR_INVALID_ARG;
+        for (int j = i + 1; j < 6; ++j)
+            if (fa::overlaps(outs[i], nouts[i], outs[j], nouts[j]))
+                return FA_ERR_INVALID_ARG;
+    }
+    if ((size_t)BH * (Tq > Tk ? Tq : Tk) == 0)
+        return FA_OK;
+    if ((st = fa::check_device()) != fa::OK)
+        return st;
+    return fa::fp8_quantize_launch(q, k, v, signs, BH, Tq, Tk, d, q8, k8, vt8, q_descale, k_descale, v_descale,
+                                   reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fa_fwd_fp8(const void *q8, const void *k8, const void *vt8, const float *q_descale, const float *k_descale,
+               const float *v_descale, void *o, float *lse, int B, int H, int Tq, int Tk, int d, int causal,
+               float scale, fa_stream_t stream)
+{
+    int st = fa::check_sizes(B, H, Tq, Tk, d, causal, scale);
+    if (st != fa::OK)
+        return st;
+    if (d != 128)
+        return FA_ERR_UNSUPPORTED;
+    const int BH = B * H;
+    const size_t nqe = (size_t)BH * Tq, nke = (size_t)BH * Tk;
+    if (!fa::present16(q8, nqe) || !fa::present16(o, nqe) || !fa::present16(lse, nqe) ||
+        !fa::present16(q_descale, nqe) || !fa::present16(k8, nke * nqe) || !fa::present16(vt8, nke * nqe) ||
+        !fa::present16(k_descale, nke * nqe) || !fa::present16(v_descale, nke * nqe))
+        return FA_ERR_INVALID_ARG;
+    const size_t no = (size_t)BH * Tq * d * 2, nl = (size_t)BH * Tq * 4;
+    const void *ins[6] = {q8, k8, vt8, q_descale, k_descale, v_descale};
+    const size_t nins[6] = {(size_t)BH * Tq * d, (size_t)BH * Tk * d, (size_t)BH * d * fa::fp8_vt_stride(Tk),
+                            (size_t)BH * ((Tq + 127) / 128) * 4, (size_t)BH * ((Tk + 127) / 128) * 4,
+                            (size_t)BH * d * 4};
+    for (int j = 0; j < 6; ++j)
+        if (fa::overlaps(o, no, ins[j], nins[j]) || fa::overlaps(lse, nl, ins[j], nins[j]))
+            return FA_ERR_INVALID_ARG;
+    if (fa::overlaps(o, no, lse, nl))
+        return FA_ERR_INVALID_ARG;
+    if ((size_t)BH * Tq == 0)
+        return FA_OK;
+    if ((st = fa::check_device()) != fa::OK)
+        return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (Tk == 0)
+        return fa::fill_empty_launch(o, lse, (size_t)BH * Tq, d, 2, s);
+    return fa::fwd_fp8_launch(q8, k8, vt8, q_descale, k_descale, v_descale, o, lse, BH, Tq, Tk, d, causal, scale, s);
 }
 
 size_t fa_decode_workspace_bytes(int B, int H, int Tq, int Tk, int d)

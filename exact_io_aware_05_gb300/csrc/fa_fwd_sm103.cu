@@ -61,11 +61,18 @@ struct FwdCfg<256> {
     static constexpr int BC = 64, NQ = 1, NSLOT = 4;
 };
 
-template <int D>
+// F8: e4m3 operands (Q, K row-major; V transposed, [channel][key]), d = 128 only.
+template <int D, bool F8 = false>
 struct FwdLayout {
     using C = FwdCfg<D>;
-    static constexpr int BC = C::BC, NQ = C::NQ, NSLOT = C::NSLOT;
-    static constexpr int KCH = D / 64;                 // 64-column (128-byte) chunks per row
+    static constexpr int BC = C::BC, NQ = C::NQ, NSLOT = F8 ? 8 : C::NSLOT;
+    static constexpr int ESZ = F8 ? 1 : 2;             // bytes per operand element
+    static constexpr int KCH = D * ESZ / 128;          // 128-byte chunks per row
+    static constexpr int CH_ELEMS = 128 / ESZ;         // elements per chunk
+    static constexpr int KSTEPS_S = D * ESZ / 32;      // S = Q K^T: 32 bytes of K per instruction
+    static constexpr int KSTEPS_PV = BC * ESZ / 32;    // O += P V: 32 bytes of keys per instruction
+    static constexpr float RESCALE = F8 ? 4.f : kRescaleLog2;
+    static_assert(!F8 || (D == 128 && BC == 128 && NQ == 2), "FP8 layout: d = 128");
     static constexpr int Q_CHUNK = BR * 128;
     static constexpr int Q_TILE = KCH * Q_CHUNK;
     static constexpr int KV_CHUNK = BC * 128;
@@ -87,8 +94,10 @@ struct FwdLayout {
     static constexpr int NTHREADS = 128 + NQ * 128;
     static_assert(O_COL + NQ * D <= TMEM_COLS, "tensor memory budget");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
-    static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BC, false, false);   // Q K^T, both K-major
-    static constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, false, true);    // P V, V is MN-major
+    static constexpr uint32_t IDESC_S =
+        F8 ? idesc_e4m3_f32(128, BC) : idesc_bf16_f32(128, BC, false, false);   // Q K^T, both K-major
+    // P V: bf16 V is MN-major ([key][channel]); the e4m3 V is stored transposed, K-major
+    static constexpr uint32_t IDESC_PV = F8 ? idesc_e4m3_f32(128, D) : idesc_bf16_f32(128, D, false, true);
 };
 
 enum WaitSite : int {
@@ -108,6 +117,10 @@ struct FwdArgs {
     int nqbm, nkbm;         // ceil(Tq / 128), ceil(Tk / 128)
     int masked;             // a left bound or a block mask: the softmax tiles do not alternate
     float scale_log2;    // scale * log2(e)
+    // FP8: dequantization factors of the e4m3 operands: Q per 128-row block, K per
+    // 128-key block, V per channel ([heads][nqd], [heads][nkd], [heads][D])
+    const float *qd, *kd, *vd;
+    int nqd, nkd;
     int nqb;             // units per head
     int units;           // BH * nqb
     int group;           // heads per L2 group
@@ -291,12 +304,13 @@ __device__ __forceinline__ bool walk_ops(int J, FS &&fs, FPV &&fpv)
     return true;
 }
 
-template <int D, bool MASKED>
-__global__ void __launch_bounds__(FwdLayout<D>::NTHREADS, 1)
+template <int D, bool MASKED, bool F8 = false>
+__global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdArgs a)
 {
-    using L = FwdLayout<D>;
+    using L = FwdLayout<D, F8>;
+    static_assert(!(F8 && MASKED), "the FP8 forward takes no window or block mask");
     constexpr int BC = L::BC, NQ = L::NQ, NSLOT = L::NSLOT;
     constexpr bool INL = MASKED && NQ == 2;   // register split below: bounded waits inlined (no calls)
     extern __shared__ uint8_t smem_raw[];
@@ -375,7 +389,7 @@ __global__ void __launch_bounds__(FwdLayout<D>::NTHREADS, 1)
                         if (tile_of(p, t).n > 0)
                             for (int c = 0; c < L::KCH; ++c)
                                 tma_load_3d_hint(sbase + L::OFF_Q + t * L::Q_TILE + c * L::Q_CHUNK, &tm_q,
-                                                 bar(L::B_QFULL), c * 64, p.row0 + t * BR, p.bh, pol_q);
+                                                 bar(L::B_QFULL), c * L::CH_ELEMS, p.row0 + t * BR, p.bh, pol_q);
                     ++n_q;
                     auto load = [&](const CUtensorMap *map, int j) -> bool {
                         const uint32_t slot = n_loads % NSLOT;
@@ -384,9 +398,12 @@ __global__ void __launch_bounds__(FwdLayout<D>::NTHREADS, 1)
                             return false;
                         mbar_arrive_expect_tx(bar(L::B_FULL + slot), L::KV_TILE);
                         const uint32_t dst = sbase + L::OFF_SLOT + slot * L::KV_TILE;
-                        for (int c = 0; c < L::KCH; ++c)
-                            tma_load_3d_hint(dst + c * L::KV_CHUNK, map, bar(L::B_FULL + slot), c * 64,
-                                             j * BC, p.bh, pol_kv);
+                        if (F8 && map == &tm_v)   // V^T: one box of BC keys x D channels
+                            tma_load_3d_hint(dst, map, bar(L::B_FULL + slot), j * BC, 0, p.bh, pol_kv);
+                        else
+                            for (int c = 0; c < L::KCH; ++c)
+                                tma_load_3d_hint(dst + c * L::KV_CHUNK, map, bar(L::B_FULL + slot), c * L::CH_ELEMS,
+                                                 j * BC, p.bh, pol_kv);
                         ++n_loads;
                         return true;
                     };
@@ -466,11 +483,14 @@ __global__ void __launch_bounds__(FwdLayout<D>::NTHREADS, 1)
                             tc_fence_after();
                             const uint32_t ka = sbase + L::OFF_SLOT + ks * L::KV_TILE;
 #pragma unroll
-                            for (int kk = 0; kk < D / 16; ++kk) {
+                            for (int kk = 0; kk < L::KSTEPS_S; ++kk) {
                                 const uint32_t off = (kk & 3) * 32;
-                                mma_ss(tmem + s_col, sdesc_sw128(qa + (kk >> 2) * L::Q_CHUNK + off, 16, 1024),
-                                       sdesc_sw128(ka + (kk >> 2) * L::KV_CHUNK + off, 16, 1024), L::IDESC_S,
-                                       kk > 0 ? 1u : 0u);
+                                const uint64_t ad = sdesc_sw128(qa + (kk >> 2) * L::Q_CHUNK + off, 16, 1024);
+                                const uint64_t bd = sdesc_sw128(ka + (kk >> 2) * L::KV_CHUNK + off, 16, 1024);
+                                if constexpr (F8)
+                                    mma_ss_f8(tmem + s_col, ad, bd, L::IDESC_S, kk > 0 ? 1u : 0u);
+                                else
+                                    mma_ss(tmem + s_col, ad, bd, L::IDESC_S, kk > 0 ? 1u : 0u);
                             }
                             tc_commit(bar(L::B_SFULL + t));
                             tc_commit(bar(L::B_EMPTY + ks));
@@ -499,9 +519,15 @@ __global__ void __launch_bounds__(FwdLayout<D>::NTHREADS, 1)
                             tc_fence_after();
                             const uint32_t va = sbase + L::OFF_SLOT + vs * L::KV_TILE;
 #pragma unroll
-                            for (int kk = 0; kk < BC / 16; ++kk)
-                                mma_ts(tmem + o_col, tmem + s_col + kk * 8, sdesc_sw128(va + kk * 16 * 128, L::KV_CHUNK, 1024),
-                                       L::IDESC_PV, (j != (MASKED ? me.first : 0) || kk > 0) ? 1u : 0u);
+                            for (int kk = 0; kk < L::KSTEPS_PV; ++kk) {
+                                const uint32_t acc = (j != (MASKED ? me.first : 0) || kk > 0) ? 1u : 0u;
+                                if constexpr (F8)   // V^T K-major: 32 keys = 32 bytes along each channel row
+                                    mma_ts_f8(tmem + o_col, tmem + s_col + kk * 8, sdesc_sw128(va + kk * 32, 16, 1024),
+                                              L::IDESC_PV, acc);
+                                else                // V MN-major: 16 keys = 16 rows of 128 bytes
+                                    mma_ts(tmem + o_col, tmem + s_col + kk * 8,
+                                           sdesc_sw128(va + kk * 16 * 128, L::KV_CHUNK, 1024), L::IDESC_PV, acc);
+                            }
                             tc_commit(bar(L::B_ODONE + t));   // O~ current and P read: one signal
                             tc_commit(bar(L::B_EMPTY + vs));
                             ++pvn;
@@ -641,6 +667,11 @@ __global__ void __launch_bounds__(FwdLayout<D>::NTHREADS, 1)
                 }
                 continue;
             }
+            // FP8: c log2(e) times the tile's Q dequantization factor; per key block the K
+            // factor joins it.  m is then kept in the exp2 domain (scores times c log2 e).
+            float sq = 1.f;
+            if constexpr (F8)
+                sq = a.scale_log2 * __ldg(a.qd + (size_t)p.bh * a.nqd + ((p.row0 + t * BR) >> 7));
             float m = -INFINITY, l = 0.f;
             bool ok = true;
             // jj: job index of this tile; j: the KV block it visits
@@ -710,20 +741,43 @@ __global__ void __launch_bounds__(FwdLayout<D>::NTHREADS, 1)
                     mx2 = fmax3(mx2, s[i + 4], s[i + 5]);
                     mx3 = fmax3(mx3, s[i + 6], s[i + 7]);
                 }
-                const float m_new = fmaxf(m, fmax3(mx0, mx1, fmax3(mx2, mx3, -INFINITY)));
-                const bool resc = (m != -INFINITY) && ((m_new - m) * sl2 > kRescaleLog2);
-                float alpha = 1.f;
-                if (m == -INFINITY) {
-                    m = m_new;                     // O~ and l of this row are still exactly 0
-                } else if (resc) {
-                    alpha = ex2_approx((m - m_new) * sl2);
-                    l *= alpha;
-                    m = m_new;
+                const float rowmax = fmax3(mx0, mx1, fmax3(mx2, mx3, -INFINITY));
+                bool resc;
+                float alpha = 1.f, mref, sl2t = sl2;
+                if constexpr (F8) {
+                    // scores scale per tile: compare in the exp2 domain.  A zero factor (an
+                    // all-zero block, whose raw scores are exactly 0) is kept positive so
+                    // that masked -inf scores stay -inf.
+                    sl2t = fmaxf(sq * __ldg(a.kd + (size_t)p.bh * a.nkd + ((j * BC) >> 7)), 1e-30f);
+                    const float m_new = fmaxf(m, rowmax * sl2t);
+                    resc = (m != -INFINITY) && (m_new - m > L::RESCALE);
+                    if (m == -INFINITY) {
+                        m = m_new;
+                    } else if (resc) {
+                        alpha = ex2_approx(m - m_new);
+                        l *= alpha;
+                        m = m_new;
+                    }
+                    // P~ carries a factor 2^4 (P~ <= 2^8 <= 448, small values stay normal in
+                    // e4m3); l carries the same factor, so O~ / l does not see it
+                    mref = (m == -INFINITY) ? 0.f : m - 4.f;
+                } else {
+                    const float m_new = fmaxf(m, rowmax);
+                    resc = (m != -INFINITY) && ((m_new - m) * sl2 > L::RESCALE);
+                    if (m == -INFINITY) {
+                        m = m_new;                     // O~ and l of this row are still exactly 0
+                    } else if (resc) {
+                        alpha = ex2_approx((m - m_new) * sl2);
+                        l *= alpha;
+                        m = m_new;
+                    }
+                    mref = (m == -INFINITY) ? 0.f : m * sl2;
                 }
                 // P~ = exp2(c log2e (s - m)), packed to bf16 pairs over the first BC/2
-                // columns of this S buffer, 32 keys at a time
-                const float mref = (m == -INFINITY) ? 0.f : m * sl2;
+                // columns of this S buffer (e4m3 quadruples over the first BC/4), 32 keys
+                // at a time
                 float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+                uint32_t pw[F8 ? BC / 4 : 1];
 #pragma unroll
                 for (int c = 0; c < BC / 32; ++c) {
                     uint32_t pk[16];
@@ -731,19 +785,26 @@ __global__ void __launch_bounds__(FwdLayout<D>::NTHREADS, 1)
                     for (int i = 0; i < 16; i += 2) {
                         const int e = c * 32 + 2 * i;
                         float x0, x1, x2, x3;
-                        ffma2(x0, x1, s[e], s[e + 1], sl2, sl2, -mref, -mref);
-                        ffma2(x2, x3, s[e + 2], s[e + 3], sl2, sl2, -mref, -mref);
+                        ffma2(x0, x1, s[e], s[e + 1], sl2t, sl2t, -mref, -mref);
+                        ffma2(x2, x3, s[e + 2], s[e + 3], sl2t, sl2t, -mref, -mref);
                         x0 = ex2_approx(x0);
                         x1 = ex2_approx(x1);
                         x2 = ex2_approx(x2);
                         x3 = ex2_approx(x3);
                         fadd2(l0, l1, l0, l1, x0, x1);
                         fadd2(l2, l3, l2, l3, x2, x3);
-                        pk[i] = pack_bf16x2(x0, x1);
-                        pk[i + 1] = pack_bf16x2(x2, x3);
+                        if constexpr (F8) {
+                            pw[c * 8 + i / 2] = pack_e4m3x4(x0, x1, x2, x3);
+                        } else {
+                            pk[i] = pack_bf16x2(x0, x1);
+                            pk[i + 1] = pack_bf16x2(x2, x3);
+                        }
                     }
-                    tmem_st_x16(lane_base + L::S_COL + b * BC + c * 16, pk);
+                    if constexpr (!F8)
+                        tmem_st_x16(lane_base + L::S_COL + b * BC + c * 16, pk);
                 }
+                if constexpr (F8)
+                    tmem_st_x32(lane_base + L::S_COL + b * BC, pw);
                 l0 += l2;
                 l1 += l3;
                 l += l0 + l1;
@@ -799,6 +860,17 @@ __global__ void __launch_bounds__(FwdLayout<D>::NTHREADS, 1)
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t v[32];
                 tmem_ld_x32(lane_base + L::O_COL + t * D + c * 32, v);
+                if constexpr (F8) {   // the V dequantization factor of each channel
+                    const float4 *vd4 = reinterpret_cast<const float4 *>(a.vd + (size_t)p.bh * D + c * 32);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float4 f = __ldg(vd4 + i);
+                        v[4 * i] = __float_as_uint(__uint_as_float(v[4 * i]) * f.x);
+                        v[4 * i + 1] = __float_as_uint(__uint_as_float(v[4 * i + 1]) * f.y);
+                        v[4 * i + 2] = __float_as_uint(__uint_as_float(v[4 * i + 2]) * f.z);
+                        v[4 * i + 3] = __float_as_uint(__uint_as_float(v[4 * i + 3]) * f.w);
+                    }
+                }
                 if (row_ok) {
                     uint32_t w[16];
 #pragma unroll
@@ -810,8 +882,10 @@ __global__ void __launch_bounds__(FwdLayout<D>::NTHREADS, 1)
                         dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
                 }
             }
-            if (row_ok)
-                a.lse[grow] = l > 0.f ? (m * sl2 + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+            if (row_ok) {
+                const float m2 = F8 ? m - 4.f : m * sl2;   // exp2-domain reference of P~ and l
+                a.lse[grow] = l > 0.f ? (m2 + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+            }
             tc_fence_before();
             mbar_arrive(bar(L::B_OEMPTY + t));
             alt_base += alt;
@@ -853,6 +927,8 @@ int launch(const void *q, const void *k, const void *v, void *o, float *lse, int
     a.nkbm = (Tk + 127) / 128;
     a.masked = (mask.left >= 0 || mask.block) ? 1 : 0;
     a.scale_log2 = scale * 1.4426950408889634f;
+    a.qd = a.kd = a.vd = nullptr;
+    a.nqd = a.nkd = 0;
     a.nqb = (Tq + L::NQ * BR - 1) / (L::NQ * BR);
     a.units = BH * a.nqb;
     // heads per group: keep the group's K and V within ~48 MB of L2
@@ -868,7 +944,65 @@ int launch(const void *q, const void *k, const void *v, void *o, float *lse, int
     return cudaGetLastError() == cudaSuccess ? OK : ERR_CUDA;
 }
 
+// The FP8 forward at d = 128: e4m3 Q, K ([heads][rows][128]) and V^T ([heads][128][ld],
+// ld = fp8_vt_stride(Tk)), causal or not.
+int launch_f8(const void *q8, const void *k8, const void *vt8, const float *qd, const float *kd, const float *vd,
+              void *o, float *lse, int BH, int Tq, int Tk, int causal, float scale, cudaStream_t s)
+{
+    constexpr int D = 128;
+    using L = FwdLayout<D, true>;
+    CUtensorMap tq, tk, tv;
+    int st = encode_tmap_3d(&tq, q8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, D, Tq, BH, 128, BR);
+    if (st == OK)
+        st = encode_tmap_3d(&tk, k8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, D, Tk, BH, 128, L::BC);
+    if (st == OK)
+        st = encode_tmap_3d_strided(&tv, vt8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Tk, D, BH, fp8_vt_stride(Tk), L::BC,
+                                    D);
+    if (st != OK)
+        return st;
+    FwdArgs a;
+    a.o = static_cast<__nv_bfloat16 *>(o);
+    a.lse = lse;
+    a.BH = BH;
+    a.Tq = Tq;
+    a.Tk = Tk;
+    a.left = -1;
+    a.right = causal ? 0 : -1;
+    a.bmask = nullptr;
+    a.bm_per_head = 0;
+    a.nqbm = (Tq + 127) / 128;
+    a.nkbm = (Tk + 127) / 128;
+    a.masked = 0;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.qd = qd;
+    a.kd = kd;
+    a.vd = vd;
+    a.nqd = (Tq + 127) / 128;
+    a.nkd = (Tk + 127) / 128;
+    a.nqb = (Tq + L::NQ * BR - 1) / (L::NQ * BR);
+    a.units = BH * a.nqb;
+    const double kv_head = 2.0 * Tk * D;
+    int g = (int)(48.0 * 1024 * 1024 / (kv_head > 1 ? kv_head : 1));
+    a.group = g < 1 ? 1 : (g > BH ? BH : g);
+    a.timeout_ns = wait_timeout_ns();
+    const int grid = a.units < device_sm_count() ? a.units : device_sm_count();
+    auto kernel = fwd_kernel<D, false, true>;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES) != cudaSuccess)
+        return ERR_CUDA;
+    kernel<<<grid, L::NTHREADS, L::SMEM_BYTES, s>>>(tq, tk, tv, a);
+    return cudaGetLastError() == cudaSuccess ? OK : ERR_CUDA;
+}
+
 }  // namespace
+
+int fwd_fp8_launch(const void *q8, const void *k8, const void *vt8, const float *qd, const float *kd,
+                   const float *vd, void *o, float *lse, int BH, int Tq, int Tk, int d, int causal, float scale,
+                   cudaStream_t s)
+{
+    if (d != 128)
+        return ERR_UNSUPPORTED;
+    return launch_f8(q8, k8, vt8, qd, kd, vd, o, lse, BH, Tq, Tk, causal, scale, s);
+}
 
 int fwd_bf16_launch(const void *q, const void *k, const void *v, void *o, float *lse, int BH, int Tq,
                     int Tk, int d, const MaskSpec &mask, float scale, cudaStream_t s)

@@ -41,6 +41,19 @@ int fwd_f32_launch(const float *q, const float *k, const float *v, float *o, flo
                    int Tq, int Tk, int d, int causal, float scale, cudaStream_t s);
 int fill_empty_launch(void *o, float *lse, size_t rows, int d, int elem_bytes, cudaStream_t s);
 
+// FP8 forward (fa_fp8_sm103.cu, fa_fwd_sm103.cu): row stride in bytes of the
+// transposed V codes, the quantization pass, and the forward over its output.
+size_t fp8_vt_stride(int Tk);
+int fp8_quantize_launch(const void *q, const void *k, const void *v, const float *signs, int BH, int Tq, int Tk,
+                        int d, void *q8, void *k8, void *vt8, float *qd, float *kd, float *vd, cudaStream_t s);
+int fwd_fp8_launch(const void *q8, const void *k8, const void *vt8, const float *qd, const float *kd,
+                   const float *vd, void *o, float *lse, int BH, int Tq, int Tk, int d, int causal, float scale,
+                   cudaStream_t s);
+// encode_tmap_3d with an explicit row stride in bytes (a multiple of 16)
+int encode_tmap_3d_strided(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes,
+                           uint64_t inner, uint64_t rows, uint64_t planes, uint64_t row_stride,
+                           uint32_t box_inner, uint32_t box_rows);
+
 // Backward workspace; rows of every head are padded to Tq_pad = roundup(Tq, 128).
 struct BwdWorkspace {
     float *lse2;     // [BH][Tq_pad]    -lse * log2(e); -inf for padding rows and rows without keys

@@ -30,6 +30,12 @@ _lib.fa_fwd_masked.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, 
 _lib.fa_fwd_masked.restype = _i
 _lib.fa_bwd_masked.argtypes = [_vp] * 9 + [_i] * 7 + [_vp, _i, _i, _f, _vp, _sz, _vp]
 _lib.fa_bwd_masked.restype = _i
+_lib.fa_fp8_vt_stride.argtypes = [_i]
+_lib.fa_fp8_vt_stride.restype = _sz
+_lib.fa_fp8_quantize.argtypes = [_vp] * 4 + [_i] * 5 + [_vp] * 6 + [_vp]
+_lib.fa_fp8_quantize.restype = _i
+_lib.fa_fwd_fp8.argtypes = [_vp] * 8 + [_i] * 6 + [_f, _vp]
+_lib.fa_fwd_fp8.restype = _i
 _lib.fa_decode.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _sz, _vp]
 _lib.fa_decode.restype = _i
 _lib.fa_decode_workspace_bytes.argtypes = [_i, _i, _i, _i, _i]
@@ -264,6 +270,77 @@ def attention_forward(q, k, v, causal: bool, scale: float, stream=None, window=N
     else:
         (fa_fwd_f32 if q.dtype == torch.float32 else fa_fwd)(q, k, v, o, lse, causal, scale, stream)
     return o, lse
+
+
+def fa_fp8_vt_stride(Tk: int) -> int:
+    return int(_lib.fa_fp8_vt_stride(Tk))
+
+
+class FP8Operands(dict):
+    """Output of fa_fp8_quantize: q8, k8 [B,H,T,d] and vt8 [B,H,d,ld] e4m3 codes (uint8),
+    q_descale [B,H,ceil(Tq/128)], k_descale [B,H,ceil(Tk/128)], v_descale [B,H,d] (f32)."""
+
+
+def alloc_fp8(B, H, Tq, Tk, d, device) -> FP8Operands:
+    u8, f32 = torch.uint8, torch.float32
+    return FP8Operands(
+        q8=torch.empty((B, H, Tq, d), dtype=u8, device=device),
+        k8=torch.empty((B, H, Tk, d), dtype=u8, device=device),
+        vt8=torch.empty((B, H, d, fa_fp8_vt_stride(Tk)), dtype=u8, device=device),
+        q_descale=torch.empty((B, H, -(-Tq // 128)), dtype=f32, device=device),
+        k_descale=torch.empty((B, H, -(-Tk // 128)), dtype=f32, device=device),
+        v_descale=torch.empty((B, H, d), dtype=f32, device=device))
+
+
+def _need_fp8(x: FP8Operands, B, H, Tq, Tk, d, dev):
+    _need(x["q8"], "q8", torch.uint8, (B, H, Tq, d), dev)
+    _need(x["k8"], "k8", torch.uint8, (B, H, Tk, d), dev)
+    _need(x["vt8"], "vt8", torch.uint8, (B, H, d, fa_fp8_vt_stride(Tk)), dev)
+    _need(x["q_descale"], "q_descale", torch.float32, (B, H, -(-Tq // 128)), dev)
+    _need(x["k_descale"], "k_descale", torch.float32, (B, H, -(-Tk // 128)), dev)
+    _need(x["v_descale"], "v_descale", torch.float32, (B, H, d), dev)
+
+
+def fa_fp8_quantize(q, k, v, signs=None, out: FP8Operands = None, stream=None) -> FP8Operands:
+    """e4m3 codes and dequantization factors of bf16 q, k, v (rotated by `signs`, a
+    float32 [d] tensor of +-1 on the device, when given)."""
+    B, H, Tq, Tk, d = _shapes(q, k)
+    dev = q.device
+    _need(q, "q", torch.bfloat16, (B, H, Tq, d), dev)
+    _need(k, "k", torch.bfloat16, (B, H, Tk, d), dev)
+    _need(v, "v", torch.bfloat16, (B, H, Tk, d), dev)
+    if signs is not None:
+        _need(signs, "signs", torch.float32, (d,), dev)
+    x = alloc_fp8(B, H, Tq, Tk, d, dev) if out is None else out
+    _need_fp8(x, B, H, Tq, Tk, d, dev)
+    _check("fa_fp8_quantize", _lib.fa_fp8_quantize(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(signs), B, H, Tq, Tk, d, _ptr(x["q8"]), _ptr(x["k8"]), _ptr(x["vt8"]),
+        _ptr(x["q_descale"]), _ptr(x["k_descale"]), _ptr(x["v_descale"]), _stream(stream)))
+    return x
+
+
+def fa_fwd_fp8(x: FP8Operands, o, lse, causal: bool, scale: float, stream=None) -> None:
+    """O (bf16) and lse (f32) of attention over the dequantized FP8 operands."""
+    B, H, Tq, d = x["q8"].shape
+    Tk = x["k8"].shape[2]
+    dev = x["q8"].device
+    _need_fp8(x, B, H, Tq, Tk, d, dev)
+    _need(o, "o", torch.bfloat16, (B, H, Tq, d), dev)
+    _need(lse, "lse", torch.float32, (B, H, Tq), dev)
+    _check("fa_fwd_fp8", _lib.fa_fwd_fp8(
+        _ptr(x["q8"]), _ptr(x["k8"]), _ptr(x["vt8"]), _ptr(x["q_descale"]), _ptr(x["k_descale"]),
+        _ptr(x["v_descale"]), _ptr(o), _ptr(lse), B, H, Tq, Tk, d, int(bool(causal)), float(scale),
+        _stream(stream)))
+
+
+def attention_forward_fp8(q, k, v, causal: bool, scale: float, signs=None, stream=None):
+    """fa_fp8_quantize then fa_fwd_fp8; returns (o, lse, the FP8 operands)."""
+    x = fa_fp8_quantize(q, k, v, signs, stream=stream)
+    B, H, Tq, d = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Tq), dtype=torch.float32, device=q.device)
+    fa_fwd_fp8(x, o, lse, causal, scale, stream)
+    return o, lse, x
 
 
 def alloc_workspace(B, H, Tq, Tk, d, device) -> torch.Tensor:

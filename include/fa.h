@@ -95,6 +95,49 @@ int fa_fwd_masked(const void *q, const void *k, const void *v, void *o, float *l
                   fa_stream_t stream);
 
 /*
+ * FP8 forward (atlas.blal.pro "FlashAttention -- IO-Aware Exact Attention",
+ * "The version ladder: FA1 -> FA2 -> FA3", the FA3 entry: e4m3 tensor-core
+ * products with block quantization and incoherent processing; "Honest caveats &
+ * open questions": a precision trade-off).  Two calls: fa_fp8_quantize turns the
+ * bf16 q, k, v of fa_fwd into e4m3 codes and fp32 dequantization factors, and
+ * fa_fwd_fp8 runs the forward over them.
+ *
+ * fa_fp8_quantize: q [B][H][Tq][d], k, v [B][H][Tk][d] bf16 as in fa_fwd.
+ * signs: d fp32 values of +-1.0 in device memory (the random rotation), or NULL
+ * for none.  With signs, each row x of q and k becomes x diag(signs) H (H the
+ * Sylvester Hadamard matrix, unnormalised, in fp32), which leaves q k^T unchanged
+ * up to the factor d folded into the descales.  Then, per 128-row block of q and of
+ * k, the block's largest |value| a maps to 448: code = e4m3(x * (448 / a)), both
+ * steps rounded to fp32, the last to nearest even with saturation; descale =
+ * a / 448 (/ sqrt(d) with signs).  v gets one scale per channel over all Tk keys
+ * and is stored transposed.  Outputs (device memory, caller-owned, 16-byte
+ * aligned, overlapping nothing else):
+ *   q8 [B][H][Tq][d], k8 [B][H][Tk][d]   e4m3 codes (one byte each);
+ *   vt8 [B][H][d][fa_fp8_vt_stride(Tk)]  e4m3 codes of v transposed; the bytes of a
+ *                                        row past Tk are not written;
+ *   q_descale [B][H][ceil(Tq/128)], k_descale [B][H][ceil(Tk/128)],
+ *   v_descale [B][H][d]                  fp32.
+ * d in {64, 128, 256}; other errors as fa_fwd.
+ *
+ * fa_fwd_fp8: O and lse of attention over q^ = q8 * q_descale (per row block),
+ * k^ = k8 * k_descale, v^ = vt8^T * v_descale (per channel):
+ *     O = softmax(scale q^ k^T) v^,  lse = log sum exp(scale q^ k^T)
+ * with fa_fwd's causal convention, output layouts and empty-row rules.  The
+ * probabilities enter the P V product as e4m3 (relative rounding error at most
+ * 2^-4 each); scores and the row sums stay fp32.  d = 128 only, else
+ * FA_ERR_UNSUPPORTED.  Arguments as produced by fa_fp8_quantize with the same
+ * sizes (every buffer 16-byte aligned); o and lse must not overlap them.  With
+ * no elements (Tq = 0, or Tk = 0 for the key side) a buffer may be NULL.
+ */
+size_t fa_fp8_vt_stride(int Tk);          /* bytes per row of vt8: Tk rounded up to 16 */
+int fa_fp8_quantize(const void *q, const void *k, const void *v, const float *signs,
+                    int B, int H, int Tq, int Tk, int d, void *q8, void *k8, void *vt8,
+                    float *q_descale, float *k_descale, float *v_descale, fa_stream_t stream);
+int fa_fwd_fp8(const void *q8, const void *k8, const void *vt8, const float *q_descale,
+               const float *k_descale, const float *v_descale, void *o, float *lse,
+               int B, int H, int Tq, int Tk, int d, int causal, float scale, fa_stream_t stream);
+
+/*
  * Split-KV attention for decoding: the O and lse of fa_fwd for a few query
  * rows per head against a long key/value sequence (atlas.blal.pro
  * "FlashAttention -- IO-Aware Exact Attention", "Honest caveats & open

@@ -112,3 +112,33 @@ def test_decode_workspace_and_validation(lib):
     assert f(*args, 1, 1, 4, 64, 128, 1, float("inf"), p + (5 << 16), 1 << 16, None) == 1
     assert f(*args, 1, 1, 4, 64, 128, 2, 0.1, p + (5 << 16), 1 << 16, None) == 1      # causal flag
     assert f(*args, 1, 1, 17, 64, 128, 1, 0.1, p + (5 << 16), 1 << 16, None) in (2, 3)   # no sm_103 here: 3
+
+
+def test_fp8_host_validation(lib):
+    """FP8 entry points reject bad sizes before any device work (no GPU needed)."""
+    import ctypes
+    vp = ctypes.c_void_p
+    lib.fa_fp8_vt_stride.argtypes = [ctypes.c_int]
+    lib.fa_fp8_vt_stride.restype = ctypes.c_size_t
+    assert [lib.fa_fp8_vt_stride(t) for t in (0, 1, 16, 17, 4096)] == [0, 16, 16, 32, 4096]
+    lib.fa_fwd_fp8.argtypes = [vp] * 8 + [ctypes.c_int] * 6 + [ctypes.c_float, vp]
+    lib.fa_fwd_fp8.restype = ctypes.c_int
+    lib.fa_fp8_quantize.argtypes = [vp] * 4 + [ctypes.c_int] * 5 + [vp] * 6 + [vp]
+    lib.fa_fp8_quantize.restype = ctypes.c_int
+    p = ctypes.c_void_p(1 << 20)        # aligned, never dereferenced: every call fails validation first
+    args8 = [p] * 8
+    assert lib.fa_fwd_fp8(*args8, 1, 1, 64, 64, 64, 0, 0.1, None) == 2          # d = 64: unsupported
+    assert lib.fa_fwd_fp8(*args8, 1, 1, 64, 64, 96, 0, 0.1, None) == 2          # d = 96
+    assert lib.fa_fwd_fp8(*args8, 1, 1, 64, 64, 128, 2, 0.1, None) == 1         # causal flag
+    assert lib.fa_fwd_fp8(*args8, 1, 1, 64, 64, 128, 0, -1.0, None) == 1        # scale
+    assert lib.fa_fwd_fp8(None, *args8[1:], 1, 1, 64, 64, 128, 0, 0.1, None) == 1
+    assert lib.fa_fwd_fp8(*args8[:7], ctypes.c_void_p((1 << 20) + 4), 1, 1, 64, 64, 128, 0, 0.1, None) == 1
+    assert lib.fa_fwd_fp8(*args8, 1, 1, 0, 64, 128, 0, 0.1, None) == 0          # nothing to do
+    q = [p] * 3
+    outs = [ctypes.c_void_p((1 << 21) + (i << 24)) for i in range(6)]
+    assert lib.fa_fp8_quantize(*q, None, 1, 1, 64, 64, 100, *outs, None) == 2    # d
+    assert lib.fa_fp8_quantize(*q, None, -1, 1, 64, 64, 128, *outs, None) == 1
+    assert lib.fa_fp8_quantize(*q, ctypes.c_void_p((1 << 20) + 8), 1, 1, 64, 64, 128, *outs, None) == 1
+    overlap = [outs[0], outs[0]] + outs[2:]
+    assert lib.fa_fp8_quantize(*q, None, 1, 1, 64, 64, 128, *overlap, None) == 1
+    assert lib.fa_fp8_quantize(*q, None, 1, 1, 0, 0, 128, *outs, None) == 0
