@@ -430,6 +430,68 @@ def run_decode(args) -> None:
     print(json.dumps(line), flush=True)
 
 
+def run_fp8(args) -> None:
+    """FP8 forward on one GPU, B8 H32 N4096 d128 causal: a step is fa_fp8_quantize (rotation,
+    block scales, e4m3 codes from the bf16 q, k, v) then fa_fwd_fp8.  The metric is forward
+    TFLOP/s (4d per unmasked pair) over the whole step; the forward kernel is also timed
+    alone against the FP8 dense peak, taken as twice the measured bf16 peak (the nominal
+    FP8 / BF16 ratio).  A secondary line; the default run is the bf16 fwd+bwd workload."""
+    import torch
+    from exact_io_aware_05_gb300 import fa, inputs
+    w = inputs.WORKLOADS["fwd_fp8_b8h32_t4096_d128_causal"]
+    torch.cuda.set_device(0)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(w.seed)
+    q = torch.randn(w.shape_q, device="cuda", generator=g).to(torch.bfloat16)
+    k = torch.randn(w.shape_kv, device="cuda", generator=g).to(torch.bfloat16)
+    v = torch.randn(w.shape_kv, device="cuda", generator=g).to(torch.bfloat16)
+    signs = inputs.rotation_signs(w.d, w.seed).cuda()
+    o = torch.empty_like(q)
+    lse = torch.empty(w.shape_q[:3], device="cuda")
+    x = fa.alloc_fp8(w.B, w.H, w.Tq, w.Tk, w.d, "cuda")
+    flops = 4.0 * w.d * w.Tq * w.Tq / 2 * w.B * w.H
+    for _ in range(args.warmup):
+        fa.fa_fp8_quantize(q, k, v, signs, out=x)
+        fa.fa_fwd_fp8(x, o, lse, True, w.scale)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(0)
+    clocks.start()
+    for e in ev:
+        e[0].record()
+        fa.fa_fp8_quantize(q, k, v, signs, out=x)
+        e[1].record()
+        fa.fa_fwd_fp8(x, o, lse, True, w.scale)
+        e[2].record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if fa.fa_sync_status() != fa.FA_OK:
+        raise RuntimeError("the FP8 forward reported a device-side error")
+    ms = sum(e[0].elapsed_time(e[2]) for e in ev) / args.steps
+    q_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
+    f_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
+    peaks = measured_peaks()
+    peak8 = 2.0 * peaks["bf16_tflops"]
+    fwd_tf = flops / (f_ms * 1e-3) / 1e12
+    # quantization bytes: q, k, v read (v twice), codes written
+    n = q.numel()
+    qbytes = 2 * n * 3 + 2 * n + n * 3
+    line = {"metric": "FP8 attention forward TFLOP/s (quantization included), B8 H32 N4096 d128 causal",
+            "value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.Tq, "d": w.d, "causal": True,
+                       "rotation": "random signs + Hadamard", "l2": "no flush: q, k, v are 805 MB"},
+            "split_ms": {"quantize": q_ms, "fwd_fp8": f_ms},
+            "roofline": {"kernel": "fwd_kernel<128, false, true>", "bound": "tensor", "achieved": fwd_tf,
+                         "peak": peak8, "unit": "TFLOP/s", "frac": fwd_tf / peak8, "traffic": None,
+                         "peak_source": "2 x measured bf16 burst peak (nominal FP8/BF16 ratio), MEASURED_PEAKS.json"},
+            "quantize_roofline": {"bound": "hbm", "achieved": qbytes / (q_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
+                                  "unit": "GB/s", "frac": qbytes / (q_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]},
+            "gpu_launches": 5 * args.steps, "clocks": clk}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -441,6 +503,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode", action="store_true",
                     help="time split-KV decode (B8 H32 Tq1 Tk32768 d128) instead of the fwd+bwd step")
+    ap.add_argument("--fp8", action="store_true",
+                    help="time the FP8 forward (quantization + fa_fwd_fp8, B8 H32 N4096 d128 causal)")
     ap.add_argument("--batch", type=int, default=WORKLOAD["B"],
                     help="batch size (default 8, the benchmark workload; smaller only for profiling)")
     args = ap.parse_args()
@@ -453,6 +517,8 @@ def main():
         run_reference(args)
     elif args.decode:
         run_decode(args)
+    elif args.fp8:
+        run_fp8(args)
     else:
         run_ours(args)
     if dist_info()[2] > 1:

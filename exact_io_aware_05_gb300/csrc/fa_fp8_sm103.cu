@@ -31,43 +31,28 @@ constexpr int QB = 128;          // rows per scale block
 constexpr int QWARPS = 16;       // warps per row block: 8 rows each
 constexpr float kE4M3Max = 448.f;
 
-template <int E>
-__device__ __forceinline__ void load_bf16(const __nv_bfloat16 *p, float (&x)[E])
+// Eight consecutive bf16 values (one 16-byte load) as floats.
+__device__ __forceinline__ void unpack8(const uint4 &u, float (&x)[8])
 {
-    if constexpr (E == 2) {
-        const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162 *>(p);
-        x[0] = __bfloat162float(h.x);
-        x[1] = __bfloat162float(h.y);
-    } else if constexpr (E == 4) {
-        const uint2 u = *reinterpret_cast<const uint2 *>(p);
-        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            x[2 * i] = __bfloat162float(h[i].x);
-            x[2 * i + 1] = __bfloat162float(h[i].y);
-        }
-    } else {
-        const uint4 u = *reinterpret_cast<const uint4 *>(p);
-        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            x[2 * i] = __bfloat162float(h[i].x);
-            x[2 * i + 1] = __bfloat162float(h[i].y);
-        }
+    for (int i = 0; i < 4; ++i) {
+        x[2 * i] = __bfloat162float(h[i].x);
+        x[2 * i + 1] = __bfloat162float(h[i].y);
     }
 }
 
-// Unnormalised Walsh-Hadamard transform of one row held by a warp, lane L holding
-// elements [L*E, L*E + E): butterflies for h = 1, 2, ..., D/2 in that order, each pair
-// (i, i + h) -> (a + b, a - b) rounded to fp32; h < E inside the thread, h >= E
-// across lanes (the lane with bit h/E set holds the upper element).
-template <int E>
-__device__ __forceinline__ void fwht_row(float (&x)[E], uint32_t lane)
+// Unnormalised Walsh-Hadamard transform of one row held by TPR consecutive lanes, lane j
+// of the group holding elements [8j, 8j + 8): butterflies for h = 1, 2, 4 inside the
+// thread, then h = 8, 16, ... across lanes (the lane with bit h/8 set holds the upper
+// element), each pair (i, i + h) -> (a + b, a - b) rounded to fp32, h increasing.
+template <int TPR>
+__device__ __forceinline__ void fwht_row8(float (&x)[8], uint32_t lane)
 {
 #pragma unroll
-    for (int h = 1; h < E; h <<= 1) {
+    for (int h = 1; h < 8; h <<= 1) {
 #pragma unroll
-        for (int i = 0; i < E; ++i)
+        for (int i = 0; i < 8; ++i)
             if ((i & h) == 0) {
                 const float a = x[i], b = x[i + h];
                 x[i] = __fadd_rn(a, b);
@@ -75,10 +60,10 @@ __device__ __forceinline__ void fwht_row(float (&x)[E], uint32_t lane)
             }
     }
 #pragma unroll
-    for (int m = 1; m < 32; m <<= 1) {
+    for (int m = 1; m < TPR; m <<= 1) {
         const bool upper = (lane & (uint32_t)m) != 0;
 #pragma unroll
-        for (int i = 0; i < E; ++i) {
+        for (int i = 0; i < 8; ++i) {
             const float p = __shfl_xor_sync(0xffffffffu, x[i], m);
             x[i] = upper ? __fsub_rn(p, x[i]) : __fadd_rn(x[i], p);
         }
@@ -95,44 +80,49 @@ struct RowQuantArgs {
     int BH;
 };
 
+// 16 warps x 8 rows; a row is held by D/8 lanes, 8 elements (16 bytes) each.
 template <int D>
 __global__ void __launch_bounds__(QWARPS * 32) fp8_rows_kernel(const RowQuantArgs a)
 {
-    constexpr int E = D / 32;
-    constexpr int RPW = QB / QWARPS;          // rows per warp
-    const int z = blockIdx.z;
-    const int T = a.T[z];
+    constexpr int TPR = D / 8;                // lanes per row
+    constexpr int RPS = 32 / TPR;             // rows per warp step
+    constexpr int STEPS = (QB / QWARPS) / RPS;
+    const bool z = blockIdx.z != 0;   // selects, not run-time array indexing (keeps the args in registers)
+    const int T = z ? a.T[1] : a.T[0];
+    const __nv_bfloat16 *src = z ? a.x[1] : a.x[0];
+    uint8_t *codes = z ? a.codes[1] : a.codes[0];
+    float *descale = z ? a.descale[1] : a.descale[0];
     const int nb = (T + QB - 1) / QB;
     if ((int)blockIdx.x >= nb)
         return;
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
     const size_t bh = blockIdx.y;
-    const int r0 = blockIdx.x * QB + (int)warp * RPW;
-    float sg[E];
+    const int col = (int)(lane % TPR) * 8;
+    const int rbase = blockIdx.x * QB + (int)warp * (QB / QWARPS) + (int)(lane / TPR);
+    uint4 raw[STEPS];
 #pragma unroll
-    for (int i = 0; i < E; ++i)
-        sg[i] = a.signs ? a.signs[lane * E + i] : 1.f;
-    float x[RPW][E];
+    for (int st = 0; st < STEPS; ++st) {
+        const int r = rbase + st * RPS;
+        raw[st] = r < T ? *reinterpret_cast<const uint4 *>(src + (bh * T + r) * D + col) : make_uint4(0, 0, 0, 0);
+    }
+    float sg[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        sg[i] = a.signs ? a.signs[col + i] : 1.f;
+    float x[STEPS][8];
     float amax = 0.f;
 #pragma unroll
-    for (int rr = 0; rr < RPW; ++rr) {
-        const int r = r0 + rr;
-        if (r < T) {
-            load_bf16<E>(a.x[z] + (bh * T + r) * D + lane * E, x[rr]);
-        } else {
-#pragma unroll
-            for (int i = 0; i < E; ++i)
-                x[rr][i] = 0.f;
-        }
+    for (int st = 0; st < STEPS; ++st) {
+        unpack8(raw[st], x[st]);
         if (a.signs) {
 #pragma unroll
-            for (int i = 0; i < E; ++i)
-                x[rr][i] *= sg[i];
-            fwht_row<E>(x[rr], lane);
+            for (int i = 0; i < 8; ++i)
+                x[st][i] *= sg[i];
+            fwht_row8<TPR>(x[st], lane);
         }
 #pragma unroll
-        for (int i = 0; i < E; ++i)
-            amax = fmaxf(amax, fabsf(x[rr][i]));
+        for (int i = 0; i < 8; ++i)
+            amax = fmaxf(amax, fabsf(x[st][i]));
     }
 #pragma unroll
     for (int m = 16; m > 0; m >>= 1)
@@ -148,29 +138,39 @@ __global__ void __launch_bounds__(QWARPS * 32) fp8_rows_kernel(const RowQuantArg
     const float inv = amax > 0.f ? __fdiv_rn(kE4M3Max, amax) : 0.f;
     if (threadIdx.x == 0) {
         const float norm = a.signs ? __frsqrt_rn((float)D) : 1.f;
-        a.descale[z][bh * nb + blockIdx.x] = amax / kE4M3Max * norm;
+        descale[bh * nb + blockIdx.x] = amax / kE4M3Max * norm;
     }
 #pragma unroll
-    for (int rr = 0; rr < RPW; ++rr) {
-        const int r = r0 + rr;
+    for (int st = 0; st < STEPS; ++st) {
+        const int r = rbase + st * RPS;
         if (r >= T)
             continue;
-        uint8_t *dst = a.codes[z] + (bh * T + r) * D + lane * E;
-        if constexpr (E == 2) {
-            const uint32_t c = __nv_cvt_float2_to_fp8x2(make_float2(__fmul_rn(x[rr][0], inv), __fmul_rn(x[rr][1], inv)),
-                                                        __NV_SATFINITE, __NV_E4M3);
-            *reinterpret_cast<uint16_t *>(dst) = (uint16_t)c;
-        } else {
-            uint32_t w[E / 4];
+        uint32_t w[2];
 #pragma unroll
-            for (int i = 0; i < E / 4; ++i)
-                w[i] = pack_e4m3x4(__fmul_rn(x[rr][4 * i], inv), __fmul_rn(x[rr][4 * i + 1], inv),
-                              __fmul_rn(x[rr][4 * i + 2], inv), __fmul_rn(x[rr][4 * i + 3], inv));
-            if constexpr (E == 4)
-                *reinterpret_cast<uint32_t *>(dst) = w[0];
-            else
-                *reinterpret_cast<uint2 *>(dst) = make_uint2(w[0], w[1]);
-        }
+        for (int i = 0; i < 2; ++i)
+            w[i] = pack_e4m3x4(__fmul_rn(x[st][4 * i], inv), __fmul_rn(x[st][4 * i + 1], inv),
+                               __fmul_rn(x[st][4 * i + 2], inv), __fmul_rn(x[st][4 * i + 3], inv));
+        *reinterpret_cast<uint2 *>(codes + (bh * T + r) * D + col) = make_uint2(w[0], w[1]);
+    }
+}
+
+// A 128-key tile of V for 256 threads: D/8 threads per key row, 8 channels (16 bytes)
+// each; thread t holds channels [8 (t % TPR), +8) of RPT consecutive keys.
+template <int D>
+struct VTile {
+    static constexpr int TPR = D / 8, RG = 256 / TPR, RPT = QB / RG;
+};
+
+template <int D>
+__device__ __forceinline__ void load_vtile(const __nv_bfloat16 *__restrict__ v, size_t bh, int l0, int Tk,
+                                           uint4 (&raw)[VTile<D>::RPT])
+{
+    using V = VTile<D>;
+    const int cg = (int)threadIdx.x % V::TPR, rg = (int)threadIdx.x / V::TPR;
+#pragma unroll
+    for (int w = 0; w < V::RPT; ++w) {
+        const int l = l0 + rg * V::RPT + w;
+        raw[w] = l < Tk ? *reinterpret_cast<const uint4 *>(v + (bh * Tk + l) * D + cg * 8) : make_uint4(0, 0, 0, 0);
     }
 }
 
@@ -179,89 +179,84 @@ __global__ void __launch_bounds__(QWARPS * 32) fp8_rows_kernel(const RowQuantArg
 template <int D>
 __global__ void __launch_bounds__(256) fp8_vmax_kernel(const __nv_bfloat16 *__restrict__ v, unsigned *amax, int Tk)
 {
-    constexpr int E = D / 32;
-    const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
+    using V = VTile<D>;
     const size_t bh = blockIdx.y;
-    float m[E];
+    uint4 raw[V::RPT];
+    load_vtile<D>(v, bh, blockIdx.x * QB, Tk, raw);
+    float m[8];
 #pragma unroll
-    for (int i = 0; i < E; ++i)
+    for (int i = 0; i < 8; ++i)
         m[i] = 0.f;
-    for (int rr = (int)warp; rr < QB; rr += 8) {
-        const int l = blockIdx.x * QB + rr;
-        if (l >= Tk)
-            break;
-        float x[E];
-        load_bf16<E>(v + (bh * Tk + l) * D + lane * E, x);
 #pragma unroll
-        for (int i = 0; i < E; ++i)
+    for (int w = 0; w < V::RPT; ++w) {
+        float x[8];
+        unpack8(raw[w], x);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
             m[i] = fmaxf(m[i], fabsf(x[i]));
     }
-    __shared__ float sm[8][D];
+    __shared__ float sm[V::RG][D];
+    const int cg = (int)threadIdx.x % V::TPR, rg = (int)threadIdx.x / V::TPR;
 #pragma unroll
-    for (int i = 0; i < E; ++i)
-        sm[warp][lane * E + i] = m[i];
+    for (int i = 0; i < 8; ++i)
+        sm[rg][cg * 8 + i] = m[i];
     __syncthreads();
     for (int c = threadIdx.x; c < D; c += blockDim.x) {
         float r = 0.f;
 #pragma unroll
-        for (int w = 0; w < 8; ++w)
-            r = fmaxf(r, sm[w][c]);
+        for (int g = 0; g < V::RG; ++g)
+            r = fmaxf(r, sm[g][c]);
         atomicMax(amax + bh * D + c, __float_as_uint(r));
     }
 }
 
-// V, pass 2: codes of 128 keys x D channels, transposed into vt[bh][c][l] (row stride ld).
+// V, pass 2: codes of 128 keys x D channels, transposed into vt[bh][c][l] (row stride ld,
+// a multiple of 16): through shared memory, then 16-byte stores along the keys.  Codes
+// of keys past Tk inside the last 16-byte chunk are 0.
 template <int D>
 __global__ void __launch_bounds__(256) fp8_vquant_kernel(const __nv_bfloat16 *__restrict__ v,
                                                          const unsigned *__restrict__ amax, uint8_t *vt, int Tk,
                                                          size_t ld)
 {
-    constexpr int E = D / 32;
-    constexpr int LDS = QB + 4;                 // padded [channel][key] rows in shared memory
+    using V = VTile<D>;
+    constexpr int LDS = QB + 4;                 // bytes per [channel] row of the tile
     __shared__ __align__(16) uint8_t tile[D * LDS];
-    const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
     const size_t bh = blockIdx.y;
     const int l0 = blockIdx.x * QB;
-    float inv[E];
+    const int cg = (int)threadIdx.x % V::TPR, rg = (int)threadIdx.x / V::TPR;
+    uint4 raw[V::RPT];
+    load_vtile<D>(v, bh, l0, Tk, raw);
+    float inv[8];
 #pragma unroll
-    for (int i = 0; i < E; ++i) {
-        const float am = __uint_as_float(amax[bh * D + lane * E + i]);
+    for (int i = 0; i < 8; ++i) {
+        const float am = __uint_as_float(amax[bh * D + cg * 8 + i]);
         inv[i] = am > 0.f ? __fdiv_rn(kE4M3Max, am) : 0.f;
     }
-    for (int rr = (int)warp; rr < QB; rr += 8) {
-        const int l = l0 + rr;
-        float x[E];
-        if (l < Tk) {
-            load_bf16<E>(v + (bh * Tk + l) * D + lane * E, x);
-        } else {
+    // codes of channel cg*8 + i for keys rg*RPT .. +RPT, four keys per word
+    uint32_t cw[8][V::RPT / 4];
 #pragma unroll
-            for (int i = 0; i < E; ++i)
-                x[i] = 0.f;
-        }
+    for (int w4 = 0; w4 < V::RPT / 4; ++w4) {
+        float x[4][8];
 #pragma unroll
-        for (int i = 0; i < E; i += 2) {
-            const uint32_t c = __nv_cvt_float2_to_fp8x2(make_float2(__fmul_rn(x[i], inv[i]), __fmul_rn(x[i + 1], inv[i + 1])),
-                                                        __NV_SATFINITE, __NV_E4M3);
-            tile[(lane * E + i) * LDS + rr] = (uint8_t)(c & 0xffu);
-            tile[(lane * E + i + 1) * LDS + rr] = (uint8_t)(c >> 8);
-        }
+        for (int e = 0; e < 4; ++e)
+            unpack8(raw[4 * w4 + e], x[e]);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            cw[i][w4] = pack_e4m3x4(__fmul_rn(x[0][i], inv[i]), __fmul_rn(x[1][i], inv[i]),
+                                    __fmul_rn(x[2][i], inv[i]), __fmul_rn(x[3][i], inv[i]));
     }
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int w4 = 0; w4 < V::RPT / 4; ++w4)
+            *reinterpret_cast<uint32_t *>(tile + (cg * 8 + i) * LDS + rg * V::RPT + 4 * w4) = cw[i][w4];
     __syncthreads();
-    // rows of the transposed tile: keys [l0, min(l0 + 128, Tk)) of each channel, 4 bytes a thread
-    const int nk = min(QB, Tk - l0);
-    for (int idx = threadIdx.x; idx < D * (QB / 4); idx += blockDim.x) {
-        const int c = idx / (QB / 4), w4 = idx - c * (QB / 4);
-        const int k4 = w4 * 4;
-        if (k4 >= nk)
+    for (int idx = threadIdx.x; idx < D * (QB / 16); idx += blockDim.x) {
+        const int c = idx / (QB / 16), k16 = (idx % (QB / 16)) * 16;
+        if (l0 + k16 >= Tk)
             continue;
-        const uint32_t word = *reinterpret_cast<const uint32_t *>(tile + c * LDS + k4);
-        uint8_t *dst = vt + (bh * D + c) * ld + l0 + k4;
-        if (k4 + 4 <= nk) {
-            *reinterpret_cast<uint32_t *>(dst) = word;   // ld and l0 are multiples of 16
-        } else {
-            for (int e = 0; e < nk - k4; ++e)
-                dst[e] = (uint8_t)(word >> (8 * e));
-        }
+        const uint32_t *src = reinterpret_cast<const uint32_t *>(tile + c * LDS + k16);
+        *reinterpret_cast<uint4 *>(vt + (bh * D + c) * ld + l0 + k16) = make_uint4(src[0], src[1], src[2], src[3]);
     }
 }
 

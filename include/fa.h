@@ -114,7 +114,7 @@ int fa_fwd_masked(const void *q, const void *k, const void *v, void *o, float *l
  * aligned, overlapping nothing else):
  *   q8 [B][H][Tq][d], k8 [B][H][Tk][d]   e4m3 codes (one byte each);
  *   vt8 [B][H][d][fa_fp8_vt_stride(Tk)]  e4m3 codes of v transposed; the bytes of a
- *                                        row past Tk are not written;
+ *                                        row past Tk are zero;
  *   q_descale [B][H][ceil(Tq/128)], k_descale [B][H][ceil(Tk/128)],
  *   v_descale [B][H][d]                  fp32.
  * d in {64, 128, 256}; other errors as fa_fwd.
