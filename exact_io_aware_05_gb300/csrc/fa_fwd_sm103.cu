@@ -62,10 +62,16 @@ struct FwdCfg<256> {
 };
 
 // F8: e4m3 operands (Q, K row-major; V transposed, [channel][key]), d = 128 only.
+//
+// Two query tiles (NQ = 2): P goes to shared memory (the A operand of P V), so that
+// S of the next key block can overwrite S in tensor memory as soon as the softmax has
+// read it, while P V of this block still runs.  One tile (d = 256): P is written
+// back over S in tensor memory and read from there by P V.
 template <int D, bool F8 = false>
 struct FwdLayout {
     using C = FwdCfg<D>;
-    static constexpr int BC = C::BC, NQ = C::NQ, NSLOT = F8 ? 8 : C::NSLOT;
+    static constexpr int BC = C::BC, NQ = C::NQ;
+    static constexpr bool PSM = NQ == 2;               // P in shared memory
     static constexpr int ESZ = F8 ? 1 : 2;             // bytes per operand element
     static constexpr int KCH = D * ESZ / 128;          // 128-byte chunks per row
     static constexpr int CH_ELEMS = 128 / ESZ;         // elements per chunk
@@ -77,15 +83,23 @@ struct FwdLayout {
     static constexpr int Q_TILE = KCH * Q_CHUNK;
     static constexpr int KV_CHUNK = BC * 128;
     static constexpr int KV_TILE = KCH * KV_CHUNK;
+    static constexpr int P_CHUNK = BR * 128;           // P of a tile: BR rows x BC keys, K-major,
+    static constexpr int PCH = BC * ESZ / 128;         // in 128-byte chunks of keys
+    static constexpr int P_TILE = PSM ? PCH * P_CHUNK : 0;
     static constexpr int OFF_Q = 0;
-    static constexpr int OFF_SLOT = NQ * Q_TILE;
+    static constexpr int OFF_P = NQ * Q_TILE;
+    static constexpr int OFF_SLOT = OFF_P + NQ * P_TILE;
+    // K/V ring: as many slots as the remaining shared memory holds, at most 8
+    static constexpr int NSLOT_FIT = (227 * 1024 - 1024 - 512 - OFF_SLOT) / KV_TILE;
+    static constexpr int NSLOT = PSM ? (NSLOT_FIT < 8 ? NSLOT_FIT : 8) : (F8 ? 8 : C::NSLOT);
+    static_assert(NSLOT >= 3, "K/V ring depth");
     static constexpr int OFF_BAR = OFF_SLOT + NSLOT * KV_TILE;
     // barrier indices
     static constexpr int B_FULL = 0, B_EMPTY = NSLOT, B_QFULL = 2 * NSLOT, B_QEMPTY = 2 * NSLOT + 1,
                          B_SFULL = 2 * NSLOT + 2, B_PFULL = 2 * NSLOT + 4, B_ODONE = 2 * NSLOT + 6,
                          B_OEMPTY = 2 * NSLOT + 8, B_DRAIN = 2 * NSLOT + 10, B_PREAD = 2 * NSLOT + 11,
                          B_OFINAL = 2 * NSLOT + 13, B_DRAIN1 = 2 * NSLOT + 15, B_TOKEN = 2 * NSLOT + 16,
-                         NBAR = 2 * NSLOT + 18;
+                         B_SFREE = 2 * NSLOT + 18, NBAR = 2 * NSLOT + 20;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;   // tmem base (u32), abort flag (int)
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1024-byte alignment
     static constexpr int S_COL = 0;                  // S buffer b at columns [b*BC, (b+1)*BC)
@@ -96,7 +110,8 @@ struct FwdLayout {
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
     static constexpr uint32_t IDESC_S =
         F8 ? idesc_e4m3_f32(128, BC) : idesc_bf16_f32(128, BC, false, false);   // Q K^T, both K-major
-    // P V: bf16 V is MN-major ([key][channel]); the e4m3 V is stored transposed, K-major
+    // P V: P K-major (shared or tensor memory); bf16 V is MN-major ([key][channel]), the
+    // e4m3 V is stored transposed, K-major
     static constexpr uint32_t IDESC_PV = F8 ? idesc_e4m3_f32(128, D) : idesc_bf16_f32(128, D, false, true);
 };
 
@@ -286,6 +301,32 @@ __device__ __forceinline__ void job_of(const Plan &p, int k, int &t, int &j, boo
     }
 }
 
+// Two tiles: the K/V blocks either tile of the unit visits (both walk them, each
+// skipping the blocks that are not its own).  union_next gives the first such block at
+// or after j (je + 1 if none), union_count their number.
+template <int BC, bool MASKED>
+__device__ __forceinline__ int union_next(const Plan &p, int j)
+{
+    if constexpr (MASKED)
+        while (j <= p.je && !tile_active<BC>(p.tr0, j) && !tile_active<BC>(p.tr1, j))
+            ++j;
+    return j;
+}
+
+template <int BC, bool MASKED>
+__device__ __forceinline__ int union_count(const Plan &p)
+{
+    if constexpr (!MASKED)
+        return p.je - p.js + 1;
+    int n = 0;
+    for (int j = union_next<BC, MASKED>(p, p.js); j <= p.je; j = union_next<BC, MASKED>(p, j + 1))
+        ++n;
+    return n;
+}
+
+// Generic-proxy writes to shared memory (P) made visible to the tensor core's reads.
+__device__ __forceinline__ void fence_smem_to_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 // The MMA order of a unit: S(0), S(1), then PV(k) followed by S(k+2).  The
 // producer walks the same order to load tiles in first-use order.
 template <typename FS, typename FPV>
@@ -346,6 +387,8 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
         mbar_init(bar(L::B_DRAIN1), 1);
         mbar_init(bar(L::B_TOKEN), 128);       // softmax ping-pong: tile 0 done with job j
         mbar_init(bar(L::B_TOKEN + 1), 128);   //                    tile 1 done with job j
+        mbar_init(bar(L::B_SFREE), 128);       // softmax of tile 0 has read S_0 (P in shared memory)
+        mbar_init(bar(L::B_SFREE + 1), 128);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tm_q);
@@ -410,10 +453,20 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                     bool ok = true;
                     if constexpr (NQ == 2) {
                         // each tile's MMA warp consumes K_j, V_j of every block either tile visits,
-                        // in this order
-                        for (int j = p.js; j <= p.je && ok; ++j)
-                            if (!MASKED || tile_active<BC>(p.tr0, j) || tile_active<BC>(p.tr1, j))
-                                ok = load(&tm_k, j) && load(&tm_v, j);
+                        // in the order S(0), S(1), PV(0), S(2), PV(1), ...
+                        int kj = union_next<BC, MASKED>(p, p.js), vj = kj;
+                        ok = walk_ops(
+                            union_count<BC, MASKED>(p),
+                            [&](int) {
+                                const bool r = load(&tm_k, kj);
+                                kj = union_next<BC, MASKED>(p, kj + 1);
+                                return r;
+                            },
+                            [&](int) {
+                                const bool r = load(&tm_v, vj);
+                                vj = union_next<BC, MASKED>(p, vj + 1);
+                                return r;
+                            });
                     } else {
                         // one tile: its visited blocks in the MMA order S(0), S(1), PV(0), S(2), ...
                         int kj = p.tr0.first, vj = p.tr0.first;
@@ -443,14 +496,17 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
             __syncwarp();
         } else if (NQ == 2 && (warp == 1 || warp == 2)) {
             // ------------------------------------------------ MMA issuer of query tile t
-            // One issuing thread per tile: a single thread cannot issue tcgen05.mma fast enough
-            // to keep the tensor core busy with N = 128 products, two interleave.
+            // One issuing thread per tile.  Both walk the K/V blocks either tile visits in the
+            // producer's order S(0), S(1), PV(0), S(2), PV(1), ...: with P in shared memory, S of
+            // block k+1 only waits for the softmax to have read S of block k, and runs while
+            // P V of block k waits for its P.
             if (lane == 0) {
                 const int t = (int)warp - 1;
                 const uint32_t s_col = L::S_COL + t * BC, o_col = L::O_COL + t * D;
-                const uint32_t qa = sbase + L::OFF_Q + t * L::Q_TILE;
+                const uint64_t qd = sdesc_sw128(sbase + L::OFF_Q + t * L::Q_TILE, 16, 1024);
+                const uint64_t pd = sdesc_sw128(sbase + L::OFF_P + t * L::P_TILE, 16, 1024);
                 const uint32_t drain_bar = bar(t == 0 ? L::B_DRAIN : L::B_DRAIN1);
-                uint32_t ld = 0, q_seen = 0, pvn = 0, epi = 0;
+                uint32_t ld = 0, q_seen = 0, sn = 0, pvn = 0, epi = 0;
                 bool ok = true;
                 for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
                     const Plan p = make_plan<D, MASKED>(u, a);
@@ -459,74 +515,84 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                     if (!mbar_wait<INL>(bar(L::B_QFULL), q_seen & 1, ctx, SITE_M_QFULL))
                         break;
                     ++q_seen;
-                    const TileRange me = tile_of(p, t), other = tile_of(p, 1 - t);
+                    const TileRange me = tile_of(p, t);
                     if (me.n == 0)
                         mbar_arrive(bar(L::B_QEMPTY));      // this tile reads no Q in this unit
-                    for (int j = p.js; j <= p.je; ++j) {
-                        const bool mine = MASKED ? tile_active<BC>(me, j) : j < me.n;
-                        if (MASKED && !mine && !tile_active<BC>(other, j))
-                            continue;                        // no tile visits block j: not loaded
-                        // K_j: S_t = Q_t K_j^T
-                        const uint32_t ks = ld % NSLOT;
-                        if (!mbar_wait<INL>(bar(L::B_FULL + ks), (ld / NSLOT) & 1, ctx, SITE_M_FULL)) {
-                            ok = false;
-                            break;
-                        }
+                    auto mine = [&](int j) { return MASKED ? tile_active<BC>(me, j) : j < me.n; };
+                    auto acquire = [&](uint32_t &slot) -> bool {
+                        slot = ld % NSLOT;
+                        const bool r = mbar_wait<INL>(bar(L::B_FULL + slot), (ld / NSLOT) & 1, ctx, SITE_M_FULL);
                         ++ld;
-                        if (mine) {
-                            // S_t overwrites the columns from which the previous PV of this tile
-                            // read P: that PV must have completed
-                            if (pvn > 0 && !mbar_wait<INL>(bar(L::B_ODONE + t), (pvn - 1) & 1, ctx, SITE_M_PREAD)) {
-                                ok = false;
-                                break;
+                        return r;
+                    };
+                    int kj = union_next<BC, MASKED>(p, p.js), vj = kj;
+                    ok = walk_ops(
+                        union_count<BC, MASKED>(p),
+                        [&](int) -> bool {
+                            // K_j: S_t = Q_t K_j^T
+                            uint32_t ks;
+                            if (!acquire(ks))
+                                return false;
+                            const int j = kj;
+                            kj = union_next<BC, MASKED>(p, kj + 1);
+                            if (!mine(j)) {
+                                mbar_arrive(bar(L::B_EMPTY + ks));   // K_j is only for the other tile
+                                return true;
                             }
+                            // S_t is overwritten once the softmax has read the previous S_t
+                            if (sn > 0 && !mbar_wait<INL>(bar(L::B_SFREE + t), (sn - 1) & 1, ctx, SITE_M_PREAD))
+                                return false;
                             tc_fence_after();
-                            const uint32_t ka = sbase + L::OFF_SLOT + ks * L::KV_TILE;
+                            // descriptors: bases once, then compile-time offsets (address field in
+                            // 16-byte units), so that the issuing thread spends no time between MMAs
+                            const uint64_t kd = sdesc_sw128(sbase + L::OFF_SLOT + ks * L::KV_TILE, 16, 1024);
 #pragma unroll
                             for (int kk = 0; kk < L::KSTEPS_S; ++kk) {
-                                const uint32_t off = (kk & 3) * 32;
-                                const uint64_t ad = sdesc_sw128(qa + (kk >> 2) * L::Q_CHUNK + off, 16, 1024);
-                                const uint64_t bd = sdesc_sw128(ka + (kk >> 2) * L::KV_CHUNK + off, 16, 1024);
+                                const uint32_t off = ((kk >> 2) * L::Q_CHUNK + (kk & 3) * 32) >> 4;
+                                const uint32_t offk = ((kk >> 2) * L::KV_CHUNK + (kk & 3) * 32) >> 4;
                                 if constexpr (F8)
-                                    mma_ss_f8(tmem + s_col, ad, bd, L::IDESC_S, kk > 0 ? 1u : 0u);
+                                    mma_ss_f8(tmem + s_col, qd + off, kd + offk, L::IDESC_S, kk > 0 ? 1u : 0u);
                                 else
-                                    mma_ss(tmem + s_col, ad, bd, L::IDESC_S, kk > 0 ? 1u : 0u);
+                                    mma_ss(tmem + s_col, qd + off, kd + offk, L::IDESC_S, kk > 0 ? 1u : 0u);
                             }
                             tc_commit(bar(L::B_SFULL + t));
                             tc_commit(bar(L::B_EMPTY + ks));
                             if (j == me.last)
                                 tc_commit(bar(L::B_QEMPTY));
-                        } else {
-                            mbar_arrive(bar(L::B_EMPTY + ks));  // K_j is only for the other tile
-                        }
-                        // V_j: O_t += P_t V_j
-                        const uint32_t vs = ld % NSLOT;
-                        if (!mbar_wait<INL>(bar(L::B_FULL + vs), (ld / NSLOT) & 1, ctx, SITE_M_FULL)) {
-                            ok = false;
-                            break;
-                        }
-                        ++ld;
-                        if (mine) {
-                            if (!mbar_wait<INL>(bar(L::B_PFULL + t), pvn & 1, ctx, SITE_M_PFULL)) {
-                                ok = false;
-                                break;
+                            ++sn;
+                            return true;
+                        },
+                        [&](int) -> bool {
+                            // V_j: O_t += P_t V_j, P_t from shared memory
+                            uint32_t vs;
+                            if (!acquire(vs))
+                                return false;
+                            const int j = vj;
+                            vj = union_next<BC, MASKED>(p, vj + 1);
+                            if (!mine(j)) {
+                                mbar_arrive(bar(L::B_EMPTY + vs));
+                                return true;
                             }
-                            if (j == (MASKED ? me.first : 0) && epi > 0 &&
-                                !mbar_wait<INL>(bar(L::B_OEMPTY + t), (epi - 1) & 1, ctx, SITE_M_OEMPTY)) {
-                                ok = false;
-                                break;
-                            }
+                            if (!mbar_wait<INL>(bar(L::B_PFULL + t), pvn & 1, ctx, SITE_M_PFULL))
+                                return false;
+                            const bool first = j == (MASKED ? me.first : 0);
+                            if (first && epi > 0 &&
+                                !mbar_wait<INL>(bar(L::B_OEMPTY + t), (epi - 1) & 1, ctx, SITE_M_OEMPTY))
+                                return false;
                             tc_fence_after();
+                            // P: K-major, 32 bytes of keys per step; V^T (FP8) K-major likewise, bf16 V
+                            // MN-major: 16 keys = 16 rows of 128 bytes
                             const uint32_t va = sbase + L::OFF_SLOT + vs * L::KV_TILE;
+                            const uint64_t vd = F8 ? sdesc_sw128(va, 16, 1024) : sdesc_sw128(va, L::KV_CHUNK, 1024);
 #pragma unroll
                             for (int kk = 0; kk < L::KSTEPS_PV; ++kk) {
-                                const uint32_t acc = (j != (MASKED ? me.first : 0) || kk > 0) ? 1u : 0u;
-                                if constexpr (F8)   // V^T K-major: 32 keys = 32 bytes along each channel row
-                                    mma_ts_f8(tmem + o_col, tmem + s_col + kk * 8, sdesc_sw128(va + kk * 32, 16, 1024),
-                                              L::IDESC_PV, acc);
-                                else                // V MN-major: 16 keys = 16 rows of 128 bytes
-                                    mma_ts(tmem + o_col, tmem + s_col + kk * 8,
-                                           sdesc_sw128(va + kk * 16 * 128, L::KV_CHUNK, 1024), L::IDESC_PV, acc);
+                                const uint32_t offp = ((kk >> 2) * L::P_CHUNK + (kk & 3) * 32) >> 4;
+                                const uint32_t offv = (F8 ? kk * 32 : kk * 16 * 128) >> 4;
+                                const uint32_t acc = (!first || kk > 0) ? 1u : 0u;
+                                if constexpr (F8)
+                                    mma_ss_f8(tmem + o_col, pd + offp, vd + offv, L::IDESC_PV, acc);
+                                else
+                                    mma_ss(tmem + o_col, pd + offp, vd + offv, L::IDESC_PV, acc);
                             }
                             tc_commit(bar(L::B_ODONE + t));   // O~ current and P read: one signal
                             tc_commit(bar(L::B_EMPTY + vs));
@@ -535,10 +601,8 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                                 tc_commit(bar(L::B_OFINAL + t));
                                 ++epi;
                             }
-                        } else {
-                            mbar_arrive(bar(L::B_EMPTY + vs));
-                        }
-                    }
+                            return true;
+                        });
                 }
                 tc_commit(drain_bar);
                 mbar_wait_drain(drain_bar, 0, a.timeout_ns);
@@ -578,14 +642,13 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                             if (g >= 2 && !mbar_wait<INL>(bar(L::B_PREAD + b), ((g - 2) >> 1) & 1, ctx, SITE_M_PREAD))
                                 return false;
                             tc_fence_after();
-                            const uint32_t qa = sbase + L::OFF_Q + t * L::Q_TILE;
-                            const uint32_t ka = sbase + L::OFF_SLOT + kslot * L::KV_TILE;
+                            const uint64_t qd = sdesc_sw128(sbase + L::OFF_Q + t * L::Q_TILE, 16, 1024);
+                            const uint64_t kd = sdesc_sw128(sbase + L::OFF_SLOT + kslot * L::KV_TILE, 16, 1024);
 #pragma unroll
-                            for (int kk = 0; kk < D / 16; ++kk) {
-                                const uint32_t off = (kk & 3) * 32;   // 16 bf16 = 32 bytes along K
-                                const uint64_t ad = sdesc_sw128(qa + (kk >> 2) * L::Q_CHUNK + off, 16, 1024);
-                                const uint64_t bd = sdesc_sw128(ka + (kk >> 2) * L::KV_CHUNK + off, 16, 1024);
-                                mma_ss(tmem + L::S_COL + b * BC, ad, bd, L::IDESC_S, kk > 0 ? 1u : 0u);
+                            for (int kk = 0; kk < D / 16; ++kk) {   // 16 bf16 = 32 bytes along K
+                                const uint32_t off = ((kk >> 2) * L::Q_CHUNK + (kk & 3) * 32) >> 4;
+                                const uint32_t offk = ((kk >> 2) * L::KV_CHUNK + (kk & 3) * 32) >> 4;
+                                mma_ss(tmem + L::S_COL + b * BC, qd + off, kd + offk, L::IDESC_S, kk > 0 ? 1u : 0u);
                             }
                             tc_commit(bar(L::B_SFULL + b));
                             if (last)
@@ -607,12 +670,17 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                                 !mbar_wait<INL>(bar(L::B_OEMPTY + t), (epi[t] - 1) & 1, ctx, SITE_M_OEMPTY))
                                 return false;
                             tc_fence_after();
-                            const uint32_t va = sbase + L::OFF_SLOT + vslot * L::KV_TILE;
+                            const uint64_t vd = sdesc_sw128(sbase + L::OFF_SLOT + vslot * L::KV_TILE, L::KV_CHUNK, 1024);
+                            if (j == 0) {
 #pragma unroll
-                            for (int kk = 0; kk < BC / 16; ++kk) {
-                                const uint64_t bd = sdesc_sw128(va + kk * 16 * 128, L::KV_CHUNK, 1024);
-                                mma_ts(tmem + L::O_COL + t * D, tmem + L::S_COL + b * BC + kk * 8, bd,
-                                       L::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+                                for (int kk = 0; kk < BC / 16; ++kk)
+                                    mma_ts(tmem + L::O_COL + t * D, tmem + L::S_COL + b * BC + kk * 8,
+                                           vd + ((kk * 16 * 128) >> 4), L::IDESC_PV, kk > 0 ? 1u : 0u);
+                            } else {
+#pragma unroll
+                                for (int kk = 0; kk < BC / 16; ++kk)
+                                    mma_ts(tmem + L::O_COL + t * D, tmem + L::S_COL + b * BC + kk * 8,
+                                           vd + ((kk * 16 * 128) >> 4), L::IDESC_PV, 1u);
                             }
                             tc_commit(bar(L::B_ODONE + t));
                             tc_commit(bar(L::B_PREAD + b));
@@ -704,6 +772,10 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
 #pragma unroll
                 for (int c = 0; c < BC / 32; ++c)
                     tmem_wait_ld_x32(sv[c]);
+                if constexpr (L::PSM) {   // S_t is in registers: the next S may overwrite it
+                    tc_fence_before();
+                    mbar_arrive(bar(L::B_SFREE + t));
+                }
                 float s[BC];
 #pragma unroll
                 for (int c = 0; c < BC / 32; ++c)
@@ -773,9 +845,18 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                     }
                     mref = (m == -INFINITY) ? 0.f : m * sl2;
                 }
-                // P~ = exp2(c log2e (s - m)), packed to bf16 pairs over the first BC/2
-                // columns of this S buffer (e4m3 quadruples over the first BC/4), 32 keys
-                // at a time
+                // P~ = exp2(c log2e (s - m)), 32 keys at a time, packed to bf16 pairs (e4m3
+                // quadruples): two tiles, into this tile's P buffer in shared memory (128-byte
+                // rows of keys, 16-byte units swizzled by the row, as the P V product reads
+                // them), which the previous P V of the tile must have finished reading; one
+                // tile, over the first columns of this S buffer.
+                if constexpr (L::PSM) {
+                    if (pv > 0 && !mbar_wait<INL>(bar(L::B_ODONE + t), (pv - 1) & 1, ctx, SITE_S_ODONE)) {
+                        ok = false;
+                        break;
+                    }
+                }
+                uint8_t *prow = smem + L::OFF_P + t * L::P_TILE + rit * 128;
                 float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
                 uint32_t pw[F8 ? BC / 4 : 1];
 #pragma unroll
@@ -800,17 +881,32 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                             pk[i + 1] = pack_bf16x2(x2, x3);
                         }
                     }
-                    if constexpr (!F8)
+                    if constexpr (!F8 && L::PSM) {
+                        // keys [32c, 32c + 32): chunk c / 2, units 4 (c % 2) .. + 3
+                        uint8_t *pc = prow + (c >> 1) * L::P_CHUNK;
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4) {
+                            const int unit = (c & 1) * 4 + v4;
+                            *reinterpret_cast<uint4 *>(pc + ((unit ^ (rit & 7)) << 4)) =
+                                make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                        }
+                    } else if constexpr (!F8) {
                         tmem_st_x16(lane_base + L::S_COL + b * BC + c * 16, pk);
+                    }
                 }
-                if constexpr (F8)
-                    tmem_st_x32(lane_base + L::S_COL + b * BC, pw);
+                if constexpr (F8) {   // 128 keys: one 128-byte row, units of 16 keys
+#pragma unroll
+                    for (int unit = 0; unit < 8; ++unit)
+                        *reinterpret_cast<uint4 *>(prow + ((unit ^ (rit & 7)) << 4)) =
+                            make_uint4(pw[4 * unit], pw[4 * unit + 1], pw[4 * unit + 2], pw[4 * unit + 3]);
+                }
                 l0 += l2;
                 l1 += l3;
                 l += l0 + l1;
                 if (__any_sync(0xffffffffu, resc)) {
-                    // O~ must hold the previous PV of this tile before it is rescaled
-                    if (!mbar_wait<INL>(bar(L::B_ODONE + t), (pv - 1) & 1, ctx, SITE_S_ODONE)) {
+                    // O~ must hold the previous PV of this tile before it is rescaled (two tiles:
+                    // waited for above)
+                    if (!L::PSM && !mbar_wait<INL>(bar(L::B_ODONE + t), (pv - 1) & 1, ctx, SITE_S_ODONE)) {
                         ok = false;
                         break;
                     }
@@ -839,6 +935,8 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                         }
                     }
                 }
+                if constexpr (L::PSM)
+                    fence_smem_to_async();
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(bar(L::B_PFULL + b));
@@ -848,9 +946,9 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
             }
             if (!ok)
                 break;
-            // epilogue: O = O~ / l, lse = c m + ln l.  The softmax can be up to two PVs
-            // ahead of the tensor core here, too far for a parity wait on the per-PV
-            // barrier; the per-unit barrier completes exactly once per epilogue.
+            // epilogue: O = O~ / l, lse = c m + ln l.  With one tile the softmax can be up
+            // to two PVs ahead of the tensor core here, too far for a parity wait on the
+            // per-PV barrier; the per-unit barrier completes exactly once per epilogue.
             if (!mbar_wait<INL>(bar(L::B_OFINAL + t), ep & 1, ctx, SITE_S_EPI))
                 break;
             ++ep;
