@@ -12,8 +12,8 @@
 // above the diagonal are never loaded or computed; the skip test compares the
 // first key of the block with the last query of the block ("The causal mask,
 // and the tiles you never visit").  The N x N matrices S and P never reach
-// HBM: S lives in tensor memory, P is written back over S as bf16 and fed to
-// the second MMA straight from tensor memory.
+// HBM: S lives in tensor memory; P (bf16) goes to shared memory with two query
+// tiles per CTA, or back over S in tensor memory with one, and feeds the second MMA.
 //
 // GB300 design (differs from the pages' A100/H100 kernels):
 //   * persistent CTAs, one per SM, each owning a 256-row unit (two 128-row
@@ -21,9 +21,13 @@
 //     longest-first within groups of heads sized so their K/V stay in L2;
 //   * warp 0: TMA producer (Q once per unit, K/V tiles through an NSLOT-deep
 //     ring with full/empty mbarriers);
-//   * warp 1: a single thread issues every tcgen05.mma and commit;
+//   * warps 1 and 2 (two tiles): one thread each issues the tcgen05.mma and
+//     commits of its tile, S of key block k+1 ahead of P V of block k (P lives
+//     in shared memory, so S may be overwritten once the softmax has read it);
+//     with one tile, warp 1 issues everything;
 //   * one 128-thread softmax warpgroup per query tile (thread = query row =
-//     tensor-memory lane) doing the online softmax and the epilogue;
+//     tensor-memory lane) doing the online softmax and the epilogue; the two
+//     warpgroups run independently;
 //   * the running maximum that P~, l and O~ refer to moves only when a row's
 //     maximum has grown by more than 2^8 in the exp2 domain (the rescale of
 //     O~ in tensor memory is skipped for a warp when none of its 32 rows needs
@@ -98,8 +102,8 @@ struct FwdLayout {
     static constexpr int B_FULL = 0, B_EMPTY = NSLOT, B_QFULL = 2 * NSLOT, B_QEMPTY = 2 * NSLOT + 1,
                          B_SFULL = 2 * NSLOT + 2, B_PFULL = 2 * NSLOT + 4, B_ODONE = 2 * NSLOT + 6,
                          B_OEMPTY = 2 * NSLOT + 8, B_DRAIN = 2 * NSLOT + 10, B_PREAD = 2 * NSLOT + 11,
-                         B_OFINAL = 2 * NSLOT + 13, B_DRAIN1 = 2 * NSLOT + 15, B_TOKEN = 2 * NSLOT + 16,
-                         B_SFREE = 2 * NSLOT + 18, NBAR = 2 * NSLOT + 20;
+                         B_OFINAL = 2 * NSLOT + 13, B_DRAIN1 = 2 * NSLOT + 15, B_SFREE = 2 * NSLOT + 16,
+                         NBAR = 2 * NSLOT + 18;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;   // tmem base (u32), abort flag (int)
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1024-byte alignment
     static constexpr int S_COL = 0;                  // S buffer b at columns [b*BC, (b+1)*BC)
@@ -117,7 +121,7 @@ struct FwdLayout {
 
 enum WaitSite : int {
     SITE_P_EMPTY = 1, SITE_P_QEMPTY, SITE_M_QFULL, SITE_M_FULL, SITE_M_PFULL, SITE_M_OEMPTY,
-    SITE_S_SFULL, SITE_S_ODONE, SITE_S_EPI, SITE_M_PREAD, SITE_S_TOKEN
+    SITE_S_SFULL, SITE_S_ODONE, SITE_S_EPI, SITE_M_PREAD
 };
 
 struct FwdArgs {
@@ -130,7 +134,7 @@ struct FwdArgs {
     const uint8_t *bmask;   // null, or [heads][nqbm][nkbm], nonzero = visit
     int bm_per_head;        // one mask per head (else one for all heads)
     int nqbm, nkbm;         // ceil(Tq / 128), ceil(Tk / 128)
-    int masked;             // a left bound or a block mask: the softmax tiles do not alternate
+    int masked;             // a left bound or a block mask: the MASKED instance runs
     float scale_log2;    // scale * log2(e)
     // FP8: dequantization factors of the e4m3 operands: Q per 128-row block, K per
     // 128-key block, V per channel ([heads][nqd], [heads][nkd], [heads][D])
@@ -353,7 +357,7 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
     using L = FwdLayout<D, F8>;
     static_assert(!(F8 && MASKED), "the FP8 forward takes no window or block mask");
     constexpr int BC = L::BC, NQ = L::NQ, NSLOT = L::NSLOT;
-    constexpr bool INL = MASKED && NQ == 2;   // register split below: bounded waits inlined (no calls)
+    constexpr bool INL = NQ == 2;   // register split below: bounded waits inlined (no calls)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -385,8 +389,6 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
         mbar_init(bar(L::B_OFINAL + 1), 1);
         mbar_init(bar(L::B_DRAIN), 1);
         mbar_init(bar(L::B_DRAIN1), 1);
-        mbar_init(bar(L::B_TOKEN), 128);       // softmax ping-pong: tile 0 done with job j
-        mbar_init(bar(L::B_TOKEN + 1), 128);   //                    tile 1 done with job j
         mbar_init(bar(L::B_SFREE), 128);       // softmax of tile 0 has read S_0 (P in shared memory)
         mbar_init(bar(L::B_SFREE + 1), 128);
         *abort_flag = 0;
@@ -407,12 +409,12 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
 
     uint32_t n_loads = 0, n_q = 0;   // producer counters, kept for the drain
 
-    // Register split with masks and two query tiles (launch: 384 threads x 168): the
-    // producer/MMA warpgroup keeps 72 per thread, the softmax warpgroups, which carry the
-    // mask state, take 216; 72 + 2 x 216 = 3 x 168.
+    // Register split with two query tiles (launch: 384 threads x 168): the producer/MMA
+    // warpgroup keeps 104 per thread, the softmax warpgroups take 200; 104 + 2 x 200 <=
+    // 3 x 168, with no spills in the unmasked instances.
     if (warp < 4) {
         if constexpr (INL)
-            regs_dealloc<72>();
+            regs_dealloc<104>();
         if (warp == 0) {
             // ------------------------------------------------ TMA producer
             if (lane == 0) {
@@ -704,7 +706,7 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
         }
     } else {
         if constexpr (INL)
-            regs_alloc<216>();
+            regs_alloc<200>();
         // ------------------------------------------------ softmax + epilogue
         const int t = (int)(warp - 4) >> 2;            // query tile of this warpgroup
         const uint32_t quarter = warp & 3u;            // TMEM lanes [32*quarter, +32)
@@ -712,16 +714,11 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
         const float sl2 = a.scale_log2;
         const uint32_t lane_base = tmem + ((quarter * 32u) << 16);
         uint32_t pv = 0, ep = 0;   // jobs and epilogues of this tile so far
-        // Ping-pong (two tiles, no left bound or block mask, so both tiles visit a prefix of
-        // the KV blocks): the jobs j < min(n0, n1) of a unit alternate between the two softmax
-        // warpgroups, (0,0), (1,0), (0,1), (1,1), ..., so that one computes while the other
-        // tile's MMAs run.  alt_base counts alternated jobs of earlier units (per tile).
-        uint32_t alt_base = 0;
+        // The two softmax warpgroups run unsynchronised: each follows its own tile's S.
         for (int u = blockIdx.x; u < a.units; u += gridDim.x) {
             const Plan p = make_plan<D, MASKED>(u, a);
             const int r = p.row0 + t * BR + rit;
             const TileRange me = tile_of(p, t);
-            const int alt = (NQ == 2 && !a.masked) ? min(p.tr0.n, p.tr1.n) : 0;
             const bool row_ok = r < a.Tq;
             const size_t grow = (size_t)p.bh * a.Tq + r;
             if (!me.rows)
@@ -752,16 +749,6 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                 if (!mbar_wait<INL>(bar(L::B_SFULL + b), ph, ctx, SITE_S_SFULL)) {
                     ok = false;
                     break;
-                }
-                if (NQ == 2 && jj < alt && (t == 1 || alt_base + jj > 0)) {
-                    // tile 1 waits for tile 0's softmax of the same job; tile 0 waits for tile 1's
-                    // previous alternated job, also across units, so neither token barrier can
-                    // run two phases ahead of its waiter
-                    const uint32_t other = t == 1 ? alt_base + jj : alt_base + jj - 1;
-                    if (!mbar_wait<INL>(bar(L::B_TOKEN + (1 - t)), other & 1, ctx, SITE_S_TOKEN)) {
-                        ok = false;
-                        break;
-                    }
                 }
                 tc_fence_after();
                 // S row: all column chunks in flight, one wait
@@ -940,8 +927,6 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(bar(L::B_PFULL + b));
-                if (NQ == 2 && jj < alt)
-                    mbar_arrive(bar(L::B_TOKEN + t));   // hand the softmax turn to the other tile
                 ++pv;
             }
             if (!ok)
@@ -986,7 +971,6 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
             }
             tc_fence_before();
             mbar_arrive(bar(L::B_OEMPTY + t));
-            alt_base += alt;
         }
     }
     // ---------------------------------------------------- teardown
