@@ -55,20 +55,27 @@ struct BwdLayout {
     static constexpr int KV_TILE = KCH * KV_CHUNK;
     static constexpr int Q_CHUNK = BQ * 128;
     static constexpr int Q_TILE = KCH * Q_CHUNK;
-    static constexpr int NST = D == 128 ? 2 : 3;          // Q/dO stages
-    static constexpr int ST_Q = 0, ST_DO = Q_TILE, ST_BYTES = 2 * Q_TILE;
+    // d = 128: dQ^T leaves through shared memory as bulk reduce-adds (TMA), staged in two
+    // 16 KB buffers; to make room, dO has one buffer of its own and only Q is staged
+    // ahead.  d = 64: Q and dO share each stage, dQ leaves by atomic adds.
+    static constexpr bool BULK = DQ_ALIAS;
+    static constexpr int NST = D == 128 ? 2 : 3;          // Q (and dO) stages
+    static constexpr int ST_Q = 0, ST_DO = BULK ? 0 : Q_TILE, ST_BYTES = BULK ? Q_TILE : 2 * Q_TILE;
     static constexpr int DS_CHUNK = BK * 128;            // dS^T: 128 keys x 64 queries bf16
     static constexpr int DS_TILE = (BQ / 64) * DS_CHUNK;
     static constexpr int NDS = DQ_ALIAS ? 1 : 2;         // dS^T buffers in shared memory
     static constexpr int OFF_K = 0, OFF_V = KV_TILE, OFF_ST = 2 * KV_TILE;
-    static constexpr int OFF_DS = OFF_ST + NST * ST_BYTES;
-    static constexpr int OFF_LSE = OFF_DS + NDS * DS_TILE;   // -lse log2(e) of the current block
+    static constexpr int OFF_DO = OFF_ST + NST * ST_BYTES;   // BULK: the dO buffer
+    static constexpr int OFF_DS = OFF_DO + (BULK ? Q_TILE : 0);
+    static constexpr int STG_BYTES = 32 * D * 4;             // BULK: dQ of 32 queries, fp32
+    static constexpr int OFF_STG = OFF_DS + NDS * DS_TILE;
+    static constexpr int OFF_LSE = OFF_STG + (BULK ? 2 * STG_BYTES : 0);   // -lse log2(e) of the current block
     static constexpr int OFF_DEL = OFF_LSE + BQ * 4;          // -D of the current block
     static constexpr int OFF_BAR = OFF_DEL + BQ * 4;
     enum : int {
         B_KVFULL = 0, B_KVEMPTY, B_STFULL, B_STEMPTY = B_STFULL + NST, B_SFULL = B_STEMPTY + NST,
         B_DPFULL, B_PFULL, B_DSFULL, B_DVDONE, B_DQFULL, B_DQEMPTY = B_DQFULL + 2, B_DKVFULL = B_DQEMPTY + 2,
-        B_DKVEMPTY, B_LFULL, B_DFULL, B_DRAIN, NBAR
+        B_DKVEMPTY, B_LFULL, B_DFULL, B_DRAIN, B_DOFULL, B_DOEMPTY, B_STGFULL, B_STGFREE = B_STGFULL + 2, NBAR = B_STGFREE + 2
     };
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
@@ -201,6 +208,26 @@ __device__ __forceinline__ void fence_proxy_async_smem()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Bulk reduce-add of `bytes` from shared memory into global memory by the TMA engine
+// (fp32 add, or 32-bit integer add for the fixed-point accumulator), in a bulk group.
+__device__ __forceinline__ void bulk_reduce_add_f32(void *dst, uint32_t src, uint32_t bytes)
+{
+    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(dst), "r"(src),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_reduce_add_u32(void *dst, uint32_t src, uint32_t bytes)
+{
+    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.u32 [%0], [%1], %2;" ::"l"(dst), "r"(src),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// at most one bulk group of this thread still reading shared memory
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+// every bulk group of this thread complete
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
 {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
@@ -271,6 +298,12 @@ __global__ void __launch_bounds__(512, 1)
         mbar_init(bar(L::B_PFULL), 256);
         mbar_init(bar(L::B_DSFULL), 256);
         mbar_init(bar(L::B_DVDONE), 1);
+        mbar_init(bar(L::B_DOFULL), 1);
+        mbar_init(bar(L::B_DOEMPTY), 1);   // dP and dV of the block have read dO
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(L::B_STGFULL + b), 128);   // the drain warpgroup has written a dQ chunk
+            mbar_init(bar(L::B_STGFREE + b), 1);     // the bulk reduce has read the chunk
+        }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(L::B_DQFULL + b), 1);
             mbar_init(bar(L::B_DQEMPTY + b), 128);
@@ -299,14 +332,14 @@ __global__ void __launch_bounds__(512, 1)
 
     // Register split (launch: 512 threads x 128): the producer/MMA/loader warpgroup gives
     // 32 per thread to the drain warpgroup, which holds a whole dQ^T tile (128 values per
-    // thread) so that it can return the tensor-memory columns before its atomic adds.
+    // thread) so that it can return the tensor-memory columns before it adds them.
     // 96 + 128 + 128 + 160 = 4 x 128.
     if (warp < 4) {
         regs_dealloc<96>();
         if (warp == 0 && lane == 0) {
             // -------------------------------------------------------- producer
             const uint64_t pol_keep = policy_evict_last();
-            uint32_t n_kv = 0, n_st = 0;
+            uint32_t n_kv = 0, n_st = 0;   // BULK: n_st also counts dO loads (one per block)
             bool ok = true;
             for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
                 const Unit x = make_unit<MASKED>(u, a);
@@ -327,12 +360,25 @@ __global__ void __launch_bounds__(512, 1)
                         break;
                     }
                     const uint32_t st = sbase + L::OFF_ST + s * L::ST_BYTES;
-                    mbar_arrive_expect_tx(bar(L::B_STFULL + s), 2 * L::Q_TILE);
+                    mbar_arrive_expect_tx(bar(L::B_STFULL + s), (L::BULK ? 1 : 2) * L::Q_TILE);
                     for (int c = 0; c < L::KCH; ++c) {
                         tma_load_3d_hint(st + L::ST_Q + c * L::Q_CHUNK, &tm_q, bar(L::B_STFULL + s), c * 64, i * BQ,
                                          x.bh, pol_keep);
-                        tma_load_3d_hint(st + L::ST_DO + c * L::Q_CHUNK, &tm_do, bar(L::B_STFULL + s), c * 64,
-                                         i * BQ, x.bh, pol_keep);
+                        if constexpr (!L::BULK)
+                            tma_load_3d_hint(st + L::ST_DO + c * L::Q_CHUNK, &tm_do, bar(L::B_STFULL + s), c * 64,
+                                             i * BQ, x.bh, pol_keep);
+                    }
+                    if constexpr (L::BULK) {
+                        // dO of block n_st: its one buffer is free once dP and dV of the previous
+                        // block, its readers, have completed
+                        if (n_st > 0 && !mbar_wait<true>(bar(L::B_DOEMPTY), (n_st - 1) & 1, ctx, SITE_P_STEMPTY)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(bar(L::B_DOFULL), L::Q_TILE);
+                        for (int c = 0; c < L::KCH; ++c)
+                            tma_load_3d_hint(sbase + L::OFF_DO + c * L::Q_CHUNK, &tm_do, bar(L::B_DOFULL), c * 64,
+                                             i * BQ, x.bh, pol_keep);
                     }
                     ++n_st;
                 }
@@ -341,6 +387,8 @@ __global__ void __launch_bounds__(512, 1)
             const uint32_t lo = n_st > (uint32_t)NST ? n_st - NST : 0;
             for (uint32_t i = lo; i < n_st; ++i)
                 mbar_wait_drain(bar(L::B_STFULL + i % NST), (i / NST) & 1, a.timeout_ns);
+            if (L::BULK && n_st > 0)
+                mbar_wait_drain(bar(L::B_DOFULL), (n_st - 1) & 1, a.timeout_ns);
             if (n_kv > 0)
                 mbar_wait_drain(bar(L::B_KVFULL), (n_kv - 1) & 1, a.timeout_ns);
         } else if (warp == 1 && lane == 0) {
@@ -383,17 +431,21 @@ __global__ void __launch_bounds__(512, 1)
                     break;
                 for (int i = 0; i < x.nq; ++i, ++g) {
                     const uint32_t st = stage_addr(g);
-                    const uint64_t dod_k = sdesc_sw128(st + L::ST_DO, 16, 1024);
+                    const uint32_t dos = L::BULK ? sbase + L::OFF_DO : st + L::ST_DO;   // dO(g)
+                    const uint64_t dod_k = sdesc_sw128(dos, 16, 1024);
                     const uint64_t qd_mn = sdesc_sw128(st + L::ST_Q, L::Q_CHUNK, 1024);
-                    const uint64_t dod_mn = sdesc_sw128(st + L::ST_DO, L::Q_CHUNK, 1024);
+                    const uint64_t dod_mn = sdesc_sw128(dos, L::Q_CHUNK, 1024);
                     // dP^T(g) = V_j dO^T (d = 128: into the columns of dQ^T(g-1), after its drain)
                     // and dV_j += P^T dO (after the softmax's P phase; the first block of a unit
                     // overwrites the accumulator, after the previous unit's epilogue)
-                    bool dp_done = false, dv_done = false;
+                    bool dp_done = false, dv_done = false, do_ok = !L::BULK;
                     PollClock pc;
                     while (!(dp_done && dv_done)) {
                         bool progress = false;
-                        if (!dp_done && (!L::DQ_ALIAS || g == 0 || mbar_test(bar(L::B_DQEMPTY), (g - 1) & 1))) {
+                        if (!do_ok)   // BULK: dO(g) has landed in its buffer (read by dP and dV)
+                            do_ok = mbar_test(bar(L::B_DOFULL), g & 1);
+                        if (!dp_done && do_ok &&
+                            (!L::DQ_ALIAS || g == 0 || mbar_test(bar(L::B_DQEMPTY), (g - 1) & 1))) {
                             tc_fence_after();
 #pragma unroll
                             for (int kk = 0; kk < D / 16; ++kk) {
@@ -404,7 +456,7 @@ __global__ void __launch_bounds__(512, 1)
                             tc_commit(bar(L::B_DPFULL));
                             dp_done = progress = true;
                         }
-                        if (!dv_done && mbar_test(bar(L::B_PFULL), g & 1) &&
+                        if (!dv_done && do_ok && mbar_test(bar(L::B_PFULL), g & 1) &&
                             (i > 0 || nu == 0 || mbar_test(bar(L::B_DKVEMPTY), (nu - 1) & 1))) {
                             tc_fence_after();
 #pragma unroll
@@ -423,6 +475,8 @@ __global__ void __launch_bounds__(512, 1)
                     }
                     if (!ok)
                         break;
+                    if constexpr (L::BULK)
+                        tc_commit(bar(L::B_DOEMPTY));   // dO(g) free once dP(g) and dV(g) complete
                     // dS(g) is in shared memory: dQ, then S of the next block, then dK
                     if (!mbar_wait<true>(bar(L::B_DSFULL), g & 1, ctx, SITE_M_DSFULL)) {
                         ok = false;
@@ -609,6 +663,8 @@ __global__ void __launch_bounds__(512, 1)
         const int row = (int)(quarter * 32 + lane);      // TMEM lane
         const uint32_t lane_base = tmem + ((quarter * 32u) << 16);
         uint32_t g = 0, nu = 0;
+        uint32_t stg_n = 0;                          // dQ chunks staged so far (BULK)
+        const bool lead = warp == 12 && lane == 0;   // issues the bulk reduce-adds
         bool ok = true;
         for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
             const Unit x = make_unit<MASKED>(u, a);
@@ -638,15 +694,12 @@ __global__ void __launch_bounds__(512, 1)
                 const float dsc = a.det_bound ? det_block_scale(a.det_bound[((size_t)x.bh * a.Tq_pad + qb) / BQ]) : 0.f;
                 int *iacc = reinterpret_cast<int *>(acc);
                 if constexpr (L::DQ_ALIAS) {
-                    // lane = feature, column = query: a warp adds 32 consecutive floats per
-                    // query.  The whole tile is read into registers first, so the columns go
-                    // back to the MMA before the atomic adds.
+                    // lane = feature, column = query.  The whole tile is read into registers
+                    // first, so the columns go back to the MMA at once; then four chunks of 32
+                    // queries go through shared memory ([query][feature], the accumulator's own
+                    // layout: a warp writes 32 consecutive words per query) and the TMA engine
+                    // adds each 16 KB chunk into the accumulator, off the load/store path.
                     uint32_t va[32], vb[32], vc[32], vd[32];
-                    auto add_chunk = [&](const uint32_t(&v)[32], int c) {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            atomicAdd(acc + (size_t)(c * 32 + e) * D + row, __uint_as_float(v[e]));
-                    };
                     tmem_ld_x32_nowait(lane_base + L::T_DQ, va);
                     tmem_ld_x32_nowait(lane_base + L::T_DQ + 32, vb);
                     tmem_ld_x32_nowait(lane_base + L::T_DQ + 64, vc);
@@ -657,21 +710,43 @@ __global__ void __launch_bounds__(512, 1)
                     tmem_wait_ld_x32(vd);
                     tc_fence_before();
                     mbar_arrive(bar(L::B_DQEMPTY));
-                    if (a.det_bound) {
-                        auto add_chunk_fixed = [&](const uint32_t(&v)[32], int c) {
+                    auto stage_chunk = [&](const uint32_t(&v)[32], int c) -> bool {
+                        const uint32_t sb = stg_n & 1u, use = stg_n >> 1;
+                        // the bulk reduce of this buffer's previous chunk has read it
+                        if (use > 0 && !mbar_wait<true>(bar(L::B_STGFREE + sb), (use - 1) & 1, ctx, SITE_D_DQFULL))
+                            return false;
+                        uint32_t *dst = reinterpret_cast<uint32_t *>(smem + L::OFF_STG + sb * L::STG_BYTES) + row;
+                        if (a.det_bound) {
 #pragma unroll
                             for (int e = 0; e < 32; ++e)
-                                atomicAdd(iacc + (size_t)(c * 32 + e) * D + row, __float2int_rn(__uint_as_float(v[e]) * dsc));
-                        };
-                        add_chunk_fixed(va, 0);
-                        add_chunk_fixed(vb, 1);
-                        add_chunk_fixed(vc, 2);
-                        add_chunk_fixed(vd, 3);
-                    } else {
-                        add_chunk(va, 0);
-                        add_chunk(vb, 1);
-                        add_chunk(vc, 2);
-                        add_chunk(vd, 3);
+                                dst[e * D] = (uint32_t)__float2int_rn(__uint_as_float(v[e]) * dsc);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                dst[e * D] = v[e];
+                        }
+                        fence_proxy_async_smem();
+                        mbar_arrive(bar(L::B_STGFULL + sb));
+                        if (lead) {
+                            if (!mbar_wait<true>(bar(L::B_STGFULL + sb), use & 1, ctx, SITE_D_DQFULL))
+                                return false;
+                            const uint32_t src = sbase + L::OFF_STG + sb * L::STG_BYTES;
+                            if (a.det_bound)
+                                bulk_reduce_add_u32(iacc + (size_t)c * 32 * D, src, L::STG_BYTES);
+                            else
+                                bulk_reduce_add_f32(acc + (size_t)c * 32 * D, src, L::STG_BYTES);
+                            bulk_commit();
+                            // the previous chunk (the other buffer) has been read: release it
+                            bulk_wait_read_1();
+                            if (stg_n > 0)
+                                mbar_arrive(bar(L::B_STGFREE + (sb ^ 1u)));
+                        }
+                        ++stg_n;
+                        return true;
+                    };
+                    if (!stage_chunk(va, 0) || !stage_chunk(vb, 1) || !stage_chunk(vc, 2) || !stage_chunk(vd, 3)) {
+                        ok = false;
+                        break;
                     }
                 } else {
                     // lane = query, column = feature
@@ -729,6 +804,8 @@ __global__ void __launch_bounds__(512, 1)
             mbar_arrive(bar(L::B_DKVEMPTY));
             ++nu;
         }
+        if (L::BULK && lead)
+            bulk_wait_all();   // every reduce-add has landed and read its shared memory
     }
     // ------------------------------------------------------------ teardown
     tc_fence_before();
