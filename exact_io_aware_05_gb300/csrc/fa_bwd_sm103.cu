@@ -67,9 +67,12 @@ struct BwdLayout {
     static constexpr int OFF_K = 0, OFF_V = KV_TILE, OFF_ST = 2 * KV_TILE;
     static constexpr int OFF_DO = OFF_ST + NST * ST_BYTES;   // BULK: the dO buffer
     static constexpr int OFF_DS = OFF_DO + (BULK ? Q_TILE : 0);
-    static constexpr int STG_BYTES = 32 * D * 4;             // BULK: dQ of 32 queries, fp32
+    // dQ of 32 queries (fp32) per staging buffer: d = 128, two buffers the drain warpgroup
+    // shares; d = 64, one per drain warp (a warp's TMEM lanes are 32 queries)
+    static constexpr int STG_BYTES = 32 * D * 4;
+    static constexpr int NSTG = BULK ? 2 : 4;
     static constexpr int OFF_STG = OFF_DS + NDS * DS_TILE;
-    static constexpr int OFF_LSE = OFF_STG + (BULK ? 2 * STG_BYTES : 0);   // -lse log2(e) of the current block
+    static constexpr int OFF_LSE = OFF_STG + NSTG * STG_BYTES;   // -lse log2(e) of the current block
     static constexpr int OFF_DEL = OFF_LSE + BQ * 4;          // -D of the current block
     static constexpr int OFF_BAR = OFF_DEL + BQ * 4;
     enum : int {
@@ -225,6 +228,8 @@ __device__ __forceinline__ void bulk_reduce_add_u32(void *dst, uint32_t src, uin
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // at most one bulk group of this thread still reading shared memory
 __device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+// no bulk group of this thread still reading shared memory
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 // every bulk group of this thread complete
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
@@ -749,26 +754,46 @@ __global__ void __launch_bounds__(512, 1)
                         break;
                     }
                 } else {
-                    // lane = query, column = feature
+                    // lane = query, column = feature: each drain warp holds the 32 queries of its
+                    // TMEM lanes, writes them into its own staging buffer ([query][feature], a
+                    // 256-byte row per thread) and its lane 0 hands the 8 KB to the TMA engine as a
+                    // bulk reduce-add.  The buffer's previous reduce-add (one block earlier) has
+                    // long finished reading it; lane 0 confirms before the warp writes.
+                    uint32_t v[L::DQ_COLS / 32][32];
 #pragma unroll
-                    for (int c = 0; c < L::DQ_COLS / 32; ++c) {
-                        uint32_t v[32];
-                        tmem_ld_x32(lane_base + L::T_DQ + b * L::DQ_COLS + c * 32, v);
-                        if (a.det_bound) {
-                            int *dst = iacc + (size_t)row * D + c * 32;
+                    for (int c = 0; c < L::DQ_COLS / 32; ++c)
+                        tmem_ld_x32_nowait(lane_base + L::T_DQ + b * L::DQ_COLS + c * 32, v[c]);
 #pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                atomicAdd(dst + e, __float2int_rn(__uint_as_float(v[e]) * dsc));
-                        } else {
-                            float4 *dst = reinterpret_cast<float4 *>(acc + (size_t)row * D + c * 32);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e)
-                                atomicAdd(dst + e, make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
-                                                               __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3])));
-                        }
-                    }
+                    for (int c = 0; c < L::DQ_COLS / 32; ++c)
+                        tmem_wait_ld_x32(v[c]);
                     tc_fence_before();
                     mbar_arrive(bar(L::B_DQEMPTY + b));
+                    if (lane == 0)
+                        bulk_wait_read_all();
+                    __syncwarp();
+                    uint8_t *srow = smem + L::OFF_STG + quarter * L::STG_BYTES + lane * (D * 4);
+#pragma unroll
+                    for (int c = 0; c < L::DQ_COLS / 32; ++c) {
+                        uint32_t w[32];
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            w[e] = a.det_bound ? (uint32_t)__float2int_rn(__uint_as_float(v[c][e]) * dsc) : v[c][e];
+#pragma unroll
+                        for (int u4 = 0; u4 < 8; ++u4)
+                            *reinterpret_cast<uint4 *>(srow + c * 128 + u4 * 16) =
+                                make_uint4(w[4 * u4], w[4 * u4 + 1], w[4 * u4 + 2], w[4 * u4 + 3]);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const uint32_t src = sbase + L::OFF_STG + quarter * L::STG_BYTES;
+                        const size_t off = (size_t)quarter * 32 * D;
+                        if (a.det_bound)
+                            bulk_reduce_add_u32(iacc + off, src, L::STG_BYTES);
+                        else
+                            bulk_reduce_add_f32(acc + off, src, L::STG_BYTES);
+                        bulk_commit();
+                    }
                 }
             }
             if (!ok)
@@ -804,7 +829,7 @@ __global__ void __launch_bounds__(512, 1)
             mbar_arrive(bar(L::B_DKVEMPTY));
             ++nu;
         }
-        if (L::BULK && lead)
+        if (L::BULK ? lead : lane == 0)
             bulk_wait_all();   // every reduce-add has landed and read its shared memory
     }
     // ------------------------------------------------------------ teardown
