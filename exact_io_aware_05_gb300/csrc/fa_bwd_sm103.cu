@@ -398,12 +398,13 @@ __global__ void __launch_bounds__(512, 1)
                 mbar_wait_drain(bar(L::B_KVFULL), (n_kv - 1) & 1, a.timeout_ns);
         } else if (warp == 1 && lane == 0) {
             // -------------------------------------------------------- MMA issuer
-        // Per block g the tensor core runs S(g) dP(g)|dV(g) dQ(g) S(g+1) dK(g): dP and dV go
-        // in whichever order their inputs become ready, dQ right after the softmax so that
-        // its drain starts early, and S of the next block before dK so that the next
-        // softmax starts early.  dS(g) in shared memory is rewritten by the softmax of a
-        // later block only after dP of that block has completed, and dP is issued after
-        // dK(g) and dQ(g), so the softmax's wait on dP also covers that hazard.
+        // Per block g the tensor core runs S(g) dP(g)|dV(g) S(g+1) dQ(g) dK(g): dP and dV go
+        // in whichever order their inputs become ready, S of the next block as soon as dV(g)
+        // frees its columns so that the next softmax starts early, and dQ right after the
+        // softmax's dS phase so that its drain starts early.  dS(g) in shared memory is
+        // rewritten by the softmax of a later block only after dP of that block has
+        // completed, and dP is issued after dK(g) and dQ(g), so the softmax's wait on dP
+        // also covers that hazard.
             uint32_t g = 0, nu = 0;   // global query-block and unit counters of this CTA
             bool ok = true;
             const uint32_t k_s = sbase + L::OFF_K, v_s = sbase + L::OFF_V;
@@ -482,7 +483,13 @@ __global__ void __launch_bounds__(512, 1)
                         break;
                     if constexpr (L::BULK)
                         tc_commit(bar(L::B_DOEMPTY));   // dO(g) free once dP(g) and dV(g) complete
-                    // dS(g) is in shared memory: dQ, then S of the next block, then dK
+                    // S of the next block as soon as dV(g) has read P^T from its columns, so that
+                    // the next P phase can follow this dS phase; then, once dS(g) is in shared
+                    // memory, dQ and dK
+                    if (i + 1 < x.nq && !issue_s(g + 1)) {
+                        ok = false;
+                        break;
+                    }
                     if (!mbar_wait<true>(bar(L::B_DSFULL), g & 1, ctx, SITE_M_DSFULL)) {
                         ok = false;
                         break;
@@ -507,10 +514,6 @@ __global__ void __launch_bounds__(512, 1)
                                    kk > 0 ? 1u : 0u);
                     }
                     tc_commit(bar(L::B_DQFULL + b));
-                    if (i + 1 < x.nq && !issue_s(g + 1)) {
-                        ok = false;
-                        break;
-                    }
                     // dK_j += dS^T Q  (dS^T from shared memory, K-major; Q MN-major)
 #pragma unroll
                     for (int kk = 0; kk < BQ / 16; ++kk) {
