@@ -78,7 +78,7 @@ struct BwdLayout {
     enum : int {
         B_KVFULL = 0, B_KVEMPTY, B_STFULL, B_STEMPTY = B_STFULL + NST, B_SFULL = B_STEMPTY + NST,
         B_DPFULL, B_PFULL, B_DSFULL, B_DVDONE, B_DQFULL, B_DQEMPTY = B_DQFULL + 2, B_DKVFULL = B_DQEMPTY + 2,
-        B_DKVEMPTY, B_LFULL, B_DFULL, B_DRAIN, B_DOFULL, B_DOEMPTY, B_STGFULL, B_STGFREE = B_STGFULL + 2, NBAR = B_STGFREE + 2
+        B_DKVEMPTY, B_LFULL, B_DFULL, B_DRAIN, B_DOFULL, B_DOEMPTY, NBAR
     };
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
@@ -211,6 +211,20 @@ __device__ __forceinline__ void fence_proxy_async_smem()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Named barrier 1 over the 128 threads of the drain warpgroup: plain, and with the AND of
+// a predicate (every thread gets the same answer, so all take the same branch after it).
+__device__ __forceinline__ void drain_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ bool drain_all(bool v)
+{
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+                 "bar.red.and.pred p, 1, 128, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(r)
+                 : "r"((uint32_t)v)
+                 : "memory");
+    return r != 0;
+}
+
 // Bulk reduce-add of `bytes` from shared memory into global memory by the TMA engine
 // (fp32 add, or 32-bit integer add for the fixed-point accumulator), in a bulk group.
 __device__ __forceinline__ void bulk_reduce_add_f32(void *dst, uint32_t src, uint32_t bytes)
@@ -305,10 +319,6 @@ __global__ void __launch_bounds__(512, 1)
         mbar_init(bar(L::B_DVDONE), 1);
         mbar_init(bar(L::B_DOFULL), 1);
         mbar_init(bar(L::B_DOEMPTY), 1);   // dP and dV of the block have read dO
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(bar(L::B_STGFULL + b), 128);   // the drain warpgroup has written a dQ chunk
-            mbar_init(bar(L::B_STGFREE + b), 1);     // the bulk reduce has read the chunk
-        }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(L::B_DQFULL + b), 1);
             mbar_init(bar(L::B_DQEMPTY + b), 128);
@@ -692,7 +702,10 @@ __global__ void __launch_bounds__(512, 1)
             for (int i = 0, qi = x.i0; i < x.nq; ++i, ++g, qi = MASKED ? unit_next(x, qi + 1, a.nkbm) : qi + 1) {
                 const uint32_t b = L::DQ_ALIAS ? 0u : (g & 1u);
                 const uint32_t ph = L::DQ_ALIAS ? (g & 1u) : ((g >> 1) & 1u);
-                if (!mbar_wait<true>(bar(L::B_DQFULL + b), ph, ctx, SITE_D_DQFULL)) {
+                bool got = mbar_wait<true>(bar(L::B_DQFULL + b), ph, ctx, SITE_D_DQFULL);
+                if constexpr (L::BULK)
+                    got = drain_all(got);   // one decision for the warpgroup (named barriers follow)
+                if (!got) {
                     ok = false;
                     break;
                 }
@@ -718,11 +731,14 @@ __global__ void __launch_bounds__(512, 1)
                     tmem_wait_ld_x32(vd);
                     tc_fence_before();
                     mbar_arrive(bar(L::B_DQEMPTY));
-                    auto stage_chunk = [&](const uint32_t(&v)[32], int c) -> bool {
-                        const uint32_t sb = stg_n & 1u, use = stg_n >> 1;
-                        // the bulk reduce of this buffer's previous chunk has read it
-                        if (use > 0 && !mbar_wait<true>(bar(L::B_STGFREE + sb), (use - 1) & 1, ctx, SITE_D_DQFULL))
-                            return false;
+                    // Named barrier 1 (the drain warpgroup's 128 threads, all on the same path)
+                    // orders each chunk: its buffer's previous reduce-add has read it, then every
+                    // thread has written its part.
+                    auto stage_chunk = [&](const uint32_t(&v)[32], int c) {
+                        const uint32_t sb = stg_n & 1u;
+                        if (lead && stg_n >= 2)
+                            bulk_wait_read_1();   // the chunk two back, in this buffer, has been read
+                        drain_sync();
                         uint32_t *dst = reinterpret_cast<uint32_t *>(smem + L::OFF_STG + sb * L::STG_BYTES) + row;
                         if (a.det_bound) {
 #pragma unroll
@@ -734,28 +750,21 @@ __global__ void __launch_bounds__(512, 1)
                                 dst[e * D] = v[e];
                         }
                         fence_proxy_async_smem();
-                        mbar_arrive(bar(L::B_STGFULL + sb));
+                        drain_sync();
                         if (lead) {
-                            if (!mbar_wait<true>(bar(L::B_STGFULL + sb), use & 1, ctx, SITE_D_DQFULL))
-                                return false;
                             const uint32_t src = sbase + L::OFF_STG + sb * L::STG_BYTES;
                             if (a.det_bound)
                                 bulk_reduce_add_u32(iacc + (size_t)c * 32 * D, src, L::STG_BYTES);
                             else
                                 bulk_reduce_add_f32(acc + (size_t)c * 32 * D, src, L::STG_BYTES);
                             bulk_commit();
-                            // the previous chunk (the other buffer) has been read: release it
-                            bulk_wait_read_1();
-                            if (stg_n > 0)
-                                mbar_arrive(bar(L::B_STGFREE + (sb ^ 1u)));
                         }
                         ++stg_n;
-                        return true;
                     };
-                    if (!stage_chunk(va, 0) || !stage_chunk(vb, 1) || !stage_chunk(vc, 2) || !stage_chunk(vd, 3)) {
-                        ok = false;
-                        break;
-                    }
+                    stage_chunk(va, 0);
+                    stage_chunk(vb, 1);
+                    stage_chunk(vc, 2);
+                    stage_chunk(vd, 3);
                 } else {
                     // lane = query, column = feature: each drain warp holds the 32 queries of its
                     // TMEM lanes, writes them into its own staging buffer ([query][feature], a
@@ -801,7 +810,10 @@ __global__ void __launch_bounds__(512, 1)
             }
             if (!ok)
                 break;
-            if (!mbar_wait<true>(bar(L::B_DKVFULL), nu & 1, ctx, SITE_D_DKVFULL))
+            bool kv_ok = mbar_wait<true>(bar(L::B_DKVFULL), nu & 1, ctx, SITE_D_DKVFULL);
+            if constexpr (L::BULK)
+                kv_ok = drain_all(kv_ok);
+            if (!kv_ok)
                 break;
             tc_fence_after();
 #pragma unroll
