@@ -833,19 +833,21 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                     mref = (m == -INFINITY) ? 0.f : m * sl2;
                 }
                 // P~ = exp2(c log2e (s - m)), 32 keys at a time, packed to bf16 pairs (e4m3
-                // quadruples): two tiles, into this tile's P buffer in shared memory (128-byte
+                // quadruples).  Two tiles: all of the row's P stays in registers until the
+                // previous P V of the tile has finished reading the tile's P buffer in shared
+                // memory, so that the wait overlaps the exponentials; then it is stored (128-byte
                 // rows of keys, 16-byte units swizzled by the row, as the P V product reads
-                // them), which the previous P V of the tile must have finished reading; one
-                // tile, over the first columns of this S buffer.
-                if constexpr (L::PSM) {
+                // them).  One tile: P goes over the first columns of this S buffer.
+                uint8_t *prow = smem + L::OFF_P + t * L::P_TILE + rit * 128;
+                if constexpr (F8) {   // measured faster with the wait ahead of the exponentials
                     if (pv > 0 && !mbar_wait<INL>(bar(L::B_ODONE + t), (pv - 1) & 1, ctx, SITE_S_ODONE)) {
                         ok = false;
                         break;
                     }
                 }
-                uint8_t *prow = smem + L::OFF_P + t * L::P_TILE + rit * 128;
                 float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
-                uint32_t pw[F8 ? BC / 4 : 1];
+                uint32_t pw[F8 ? BC / 4 : 1];                   // e4m3 quadruples
+                uint32_t pb[(!F8 && L::PSM) ? BC / 2 : 1];     // bf16 pairs (two tiles)
 #pragma unroll
                 for (int c = 0; c < BC / 32; ++c) {
                     uint32_t pk[16];
@@ -863,29 +865,36 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                         fadd2(l2, l3, l2, l3, x2, x3);
                         if constexpr (F8) {
                             pw[c * 8 + i / 2] = pack_e4m3x4(x0, x1, x2, x3);
+                        } else if constexpr (L::PSM) {
+                            pb[c * 16 + i] = pack_bf16x2(x0, x1);
+                            pb[c * 16 + i + 1] = pack_bf16x2(x2, x3);
                         } else {
                             pk[i] = pack_bf16x2(x0, x1);
                             pk[i + 1] = pack_bf16x2(x2, x3);
                         }
                     }
-                    if constexpr (!F8 && L::PSM) {
-                        // keys [32c, 32c + 32): chunk c / 2, units 4 (c % 2) .. + 3
-                        uint8_t *pc = prow + (c >> 1) * L::P_CHUNK;
-#pragma unroll
-                        for (int v4 = 0; v4 < 4; ++v4) {
-                            const int unit = (c & 1) * 4 + v4;
-                            *reinterpret_cast<uint4 *>(pc + ((unit ^ (rit & 7)) << 4)) =
-                                make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
-                        }
-                    } else if constexpr (!F8) {
+                    if constexpr (!F8 && !L::PSM)
                         tmem_st_x16(lane_base + L::S_COL + b * BC + c * 16, pk);
-                    }
                 }
-                if constexpr (F8) {   // 128 keys: one 128-byte row, units of 16 keys
+                if constexpr (L::PSM) {
+                    if (!F8 && pv > 0 && !mbar_wait<INL>(bar(L::B_ODONE + t), (pv - 1) & 1, ctx, SITE_S_ODONE)) {
+                        ok = false;
+                        break;
+                    }
+                    if constexpr (F8) {   // 128 keys: one 128-byte row, units of 16 keys
 #pragma unroll
-                    for (int unit = 0; unit < 8; ++unit)
-                        *reinterpret_cast<uint4 *>(prow + ((unit ^ (rit & 7)) << 4)) =
-                            make_uint4(pw[4 * unit], pw[4 * unit + 1], pw[4 * unit + 2], pw[4 * unit + 3]);
+                        for (int unit = 0; unit < 8; ++unit)
+                            *reinterpret_cast<uint4 *>(prow + ((unit ^ (rit & 7)) << 4)) =
+                                make_uint4(pw[4 * unit], pw[4 * unit + 1], pw[4 * unit + 2], pw[4 * unit + 3]);
+                    } else {              // keys [64h, 64h + 64): chunk h, units of 8 keys
+#pragma unroll
+                        for (int h = 0; h < BC / 64; ++h)
+#pragma unroll
+                            for (int unit = 0; unit < 8; ++unit)
+                                *reinterpret_cast<uint4 *>(prow + h * L::P_CHUNK + ((unit ^ (rit & 7)) << 4)) =
+                                    make_uint4(pb[h * 32 + 4 * unit], pb[h * 32 + 4 * unit + 1],
+                                               pb[h * 32 + 4 * unit + 2], pb[h * 32 + 4 * unit + 3]);
+                    }
                 }
                 l0 += l2;
                 l1 += l3;
