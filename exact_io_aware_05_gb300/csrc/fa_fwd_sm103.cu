@@ -231,54 +231,55 @@ __device__ __forceinline__ Plan make_plan(int u, const FwdArgs &a)
         p.js = 0;
         p.je = max(p.tr0.n, p.tr1.n) - 1;
         return p;
-    }
+    } else {
 #pragma unroll
-    for (int t = 0; t < 2; ++t) {
-        TileRange tr;
-        const int r_first = p.row0 + t * BR;
-        tr.rows = (t < L::NQ) && (r_first < a.Tq);
-        tr.lo = 0;
-        tr.hi = -1;
-        tr.bm = nullptr;
-        if (tr.rows) {
-            const int r_last = min(r_first + BR - 1, a.Tq - 1);
-            // keys any row of the tile may see: from the first row's lowest to the last row's highest
-            const long klo = a.left >= 0 ? max(0L, (long)r_first + off - a.left) : 0L;
-            const long khi = a.right >= 0 ? min((long)a.Tk - 1, (long)r_last + off + a.right) : (long)a.Tk - 1;
-            if (klo <= khi) {
-                tr.lo = (int)(klo / L::BC);
-                tr.hi = (int)(khi / L::BC);
-            }
-            if (a.bmask)
-                tr.bm = a.bmask + ((size_t)(a.bm_per_head ? p.bh : 0) * a.nqbm + (r_first >> 7)) * a.nkbm;
-        }
-        int n = 0;
-        if (!tr.bm) {
-            n = tr.hi - tr.lo + 1;
-            tr.first = tr.lo;
-            tr.last = tr.hi;
-        } else {
-            tr.first = tr.hi + 1;
-            tr.last = tr.lo - 1;
-            for (int j = tr.lo; j <= tr.hi; ++j)
-                if (tile_active<L::BC>(tr, j)) {
-                    tr.first = min(tr.first, j);
-                    tr.last = j;
-                    ++n;
+        for (int t = 0; t < 2; ++t) {
+            TileRange tr;
+            const int r_first = p.row0 + t * BR;
+            tr.rows = (t < L::NQ) && (r_first < a.Tq);
+            tr.lo = 0;
+            tr.hi = -1;
+            tr.bm = nullptr;
+            if (tr.rows) {
+                const int r_last = min(r_first + BR - 1, a.Tq - 1);
+                // keys any row of the tile may see: from the first row's lowest to the last row's highest
+                const long klo = a.left >= 0 ? max(0L, (long)r_first + off - a.left) : 0L;
+                const long khi = a.right >= 0 ? min((long)a.Tk - 1, (long)r_last + off + a.right) : (long)a.Tk - 1;
+                if (klo <= khi) {
+                    tr.lo = (int)(klo / L::BC);
+                    tr.hi = (int)(khi / L::BC);
                 }
+                if (a.bmask)
+                    tr.bm = a.bmask + ((size_t)(a.bm_per_head ? p.bh : 0) * a.nqbm + (r_first >> 7)) * a.nkbm;
+            }
+            int n = 0;
+            if (!tr.bm) {
+                n = tr.hi - tr.lo + 1;
+                tr.first = tr.lo;
+                tr.last = tr.hi;
+            } else {
+                tr.first = tr.hi + 1;
+                tr.last = tr.lo - 1;
+                for (int j = tr.lo; j <= tr.hi; ++j)
+                    if (tile_active<L::BC>(tr, j)) {
+                        tr.first = min(tr.first, j);
+                        tr.last = j;
+                        ++n;
+                    }
+            }
+            tr.n = n > 0 ? n : 0;
+            if (n > 0) {
+                p.js = min(p.js, tr.first);
+                p.je = max(p.je, tr.last);
+            }
+            p.J += tr.n;
+            if (t == 0)
+                p.tr0 = tr;
+            else
+                p.tr1 = tr;
         }
-        tr.n = n > 0 ? n : 0;
-        if (n > 0) {
-            p.js = min(p.js, tr.first);
-            p.je = max(p.je, tr.last);
-        }
-        p.J += tr.n;
-        if (t == 0)
-            p.tr0 = tr;
-        else
-            p.tr1 = tr;
+        return p;
     }
-    return p;
 }
 
 // Job k of a unit -> (query tile t, key block j); first/last: whether this job
