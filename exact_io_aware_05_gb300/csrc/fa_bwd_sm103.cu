@@ -20,16 +20,16 @@
 //     longest-first within groups of heads; query blocks are 128 rows, so every
 //     product is a full M128 x N128 (d = 128) tensor-core instruction;
 //   * warp 0 streams K_j, V_j once per unit and Q_i, dO_i per query block
-//     through a ring of stages (TMA); warp 1 issues all tcgen05.mma; two
-//     softmax warpgroups each rebuild half of a block's P^T and dS^T from S^T
-//     and dP^T in tensor memory (lse and D come from L1-cached global loads);
-//     a fourth warpgroup drains dQ from tensor memory into the fp32
-//     accumulator with atomic adds and writes dK, dV at the end of the unit;
+//     through a ring of stages (TMA); warp 1 issues all tcgen05.mma; warp 2
+//     stages each block's lse and D (bulk copies); two softmax warpgroups each
+//     rebuild half of a block's P^T and dS^T from S^T and dP^T in tensor
+//     memory; a fourth warpgroup drains dQ from tensor memory into the fp32
+//     accumulator through shared memory with bulk reduce-adds (TMA) and
+//     writes dK, dV at the end of the unit;
 //   * tensor memory (512 columns): S^T, dP^T (128 keys x 128 queries) and the
 //     dV, dK accumulators.  For d = 128 dQ is formed transposed
-//     (dQ^T = K_j^T dS^T, M = d) in the S^T columns once dV has read P^T
-//     from them; for d = 64, dQ = dS K_j has two buffers of its own and is
-//     issued one block late, under the next block's softmax;
+//     (dQ^T = K_j^T dS^T, M = d) in the dP^T columns once the softmax has
+//     read dP^T from them; for d = 64, dQ = dS K_j has two buffers of its own;
 //   * every MMA that overwrites a tensor-memory region waits for the MMA (or
 //     the drain) that last read it, and every wait is bounded.
 #include "fa_common.cuh"
@@ -406,15 +406,20 @@ __global__ void __launch_bounds__(512, 1)
                 mbar_wait_drain(bar(L::B_DOFULL), (n_st - 1) & 1, a.timeout_ns);
             if (n_kv > 0)
                 mbar_wait_drain(bar(L::B_KVFULL), (n_kv - 1) & 1, a.timeout_ns);
-        } else if (warp == 1 && lane == 0) {
+        } else if (warp == 1) {
             // -------------------------------------------------------- MMA issuer
-        // Per block g the tensor core runs S(g) dP(g)|dV(g) S(g+1) dQ(g) dK(g): dP and dV go
-        // in whichever order their inputs become ready, S of the next block as soon as dV(g)
-        // frees its columns so that the next softmax starts early, and dQ right after the
-        // softmax's dS phase so that its drain starts early.  dS(g) in shared memory is
-        // rewritten by the softmax of a later block only after dP of that block has
-        // completed, and dP is issued after dK(g) and dQ(g), so the softmax's wait on dP
-        // also covers that hazard.
+        // Per block g the tensor core runs dP(g) dV(g) S(g+1) dQ(g) dK(g): dP first (its inputs
+        // are ready earliest), dV once the softmax's P phase is done, S of the next block as
+        // soon as dV(g) frees its columns so that the next softmax starts early, and dQ right
+        // after the softmax's dS phase so that its drain starts early.  dS(g) in shared memory
+        // is rewritten by the softmax of a later block only after dP of that block has
+        // completed, and dP is issued after dK(g) and dQ(g), so the softmax's wait on dP also
+        // covers that hazard.
+        // The whole warp runs this loop, which keeps the descriptor arithmetic warp-uniform and
+        // measured faster than one thread alone; lane 0 issues each group of MMAs and its
+        // commit (a commit tracks the MMAs of its own thread).  Every lane waits on its own:
+        // outcomes differ only when a wait gives up, no warp-collective operation runs in the
+        // loop, and lanes that leave it at different points meet at the __syncwarp below.
             uint32_t g = 0, nu = 0;   // global query-block and unit counters of this CTA
             bool ok = true;
             const uint32_t k_s = sbase + L::OFF_K, v_s = sbase + L::OFF_V;
@@ -422,28 +427,31 @@ __global__ void __launch_bounds__(512, 1)
             const uint64_t kd_mn = sdesc_sw128(k_s, L::KV_CHUNK, 1024);
             auto stage_addr = [&](uint32_t gq) { return sbase + L::OFF_ST + (gq % NST) * L::ST_BYTES; };
             auto ds_addr = [&](uint32_t gq) { return sbase + L::OFF_DS + (L::NDS == 1 ? 0u : (gq & 1u)) * L::DS_TILE; };
+            auto wait = [&](uint32_t b, uint32_t parity, int site) { return mbar_wait<true>(b, parity, ctx, site); };
             // S^T(gq) = K_j Q^T: waits for its stage and for dV(gq-1), the last reader of P^T
             auto issue_s = [&](uint32_t gq) -> bool {
-                if (!mbar_wait<true>(bar(L::B_STFULL + gq % NST), (gq / NST) & 1, ctx, SITE_M_STFULL))
+                if (!wait(bar(L::B_STFULL + gq % NST), (gq / NST) & 1, SITE_M_STFULL))
                     return false;
-                if (gq > 0 && !mbar_wait<true>(bar(L::B_DVDONE), (gq - 1) & 1, ctx, SITE_M_DVDONE))
+                if (gq > 0 && !wait(bar(L::B_DVDONE), (gq - 1) & 1, SITE_M_DVDONE))
                     return false;
                 tc_fence_after();
                 const uint64_t qd_k = sdesc_sw128(stage_addr(gq) + L::ST_Q, 16, 1024);
+                if (lane == 0) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t ka = (uint64_t)(((kk >> 2) * L::KV_CHUNK + (kk & 3) * 32) >> 4);
-                    const uint64_t qa = (uint64_t)(((kk >> 2) * L::Q_CHUNK + (kk & 3) * 32) >> 4);
-                    mma_ss(tmem + L::T_S, kd_k + ka, qd_k + qa, L::ID_SDP, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint64_t ka = (uint64_t)(((kk >> 2) * L::KV_CHUNK + (kk & 3) * 32) >> 4);
+                        const uint64_t qa = (uint64_t)(((kk >> 2) * L::Q_CHUNK + (kk & 3) * 32) >> 4);
+                        mma_ss(tmem + L::T_S, kd_k + ka, qd_k + qa, L::ID_SDP, kk > 0 ? 1u : 0u);
+                    }
+                    tc_commit(bar(L::B_SFULL));
                 }
-                tc_commit(bar(L::B_SFULL));
                 return true;
             };
             for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
                 const Unit x = make_unit<MASKED>(u, a);
                 if (x.nq == 0)
                     continue;
-                if (!mbar_wait<true>(bar(L::B_KVFULL), nu & 1, ctx, SITE_M_KVFULL) || !issue_s(g))
+                if (!wait(bar(L::B_KVFULL), nu & 1, SITE_M_KVFULL) || !issue_s(g))
                     break;
                 for (int i = 0; i < x.nq; ++i, ++g) {
                     const uint32_t st = stage_addr(g);
@@ -451,48 +459,42 @@ __global__ void __launch_bounds__(512, 1)
                     const uint64_t dod_k = sdesc_sw128(dos, 16, 1024);
                     const uint64_t qd_mn = sdesc_sw128(st + L::ST_Q, L::Q_CHUNK, 1024);
                     const uint64_t dod_mn = sdesc_sw128(dos, L::Q_CHUNK, 1024);
-                    // dP^T(g) = V_j dO^T (d = 128: into the columns of dQ^T(g-1), after its drain)
-                    // and dV_j += P^T dO (after the softmax's P phase; the first block of a unit
-                    // overwrites the accumulator, after the previous unit's epilogue)
-                    bool dp_done = false, dv_done = false, do_ok = !L::BULK;
-                    PollClock pc;
-                    while (!(dp_done && dv_done)) {
-                        bool progress = false;
-                        if (!do_ok)   // BULK: dO(g) has landed in its buffer (read by dP and dV)
-                            do_ok = mbar_test(bar(L::B_DOFULL), g & 1);
-                        if (!dp_done && do_ok &&
-                            (!L::DQ_ALIAS || g == 0 || mbar_test(bar(L::B_DQEMPTY), (g - 1) & 1))) {
-                            tc_fence_after();
-#pragma unroll
-                            for (int kk = 0; kk < D / 16; ++kk) {
-                                const uint64_t ka = (uint64_t)(((kk >> 2) * L::KV_CHUNK + (kk & 3) * 32) >> 4);
-                                const uint64_t qa = (uint64_t)(((kk >> 2) * L::Q_CHUNK + (kk & 3) * 32) >> 4);
-                                mma_ss(tmem + L::T_DP, vd_k + ka, dod_k + qa, L::ID_SDP, kk > 0 ? 1u : 0u);
-                            }
-                            tc_commit(bar(L::B_DPFULL));
-                            dp_done = progress = true;
-                        }
-                        if (!dv_done && do_ok && mbar_test(bar(L::B_PFULL), g & 1) &&
-                            (i > 0 || nu == 0 || mbar_test(bar(L::B_DKVEMPTY), (nu - 1) & 1))) {
-                            tc_fence_after();
-#pragma unroll
-                            for (int kk = 0; kk < BQ / 16; ++kk) {
-                                const uint64_t step = (uint64_t)((kk * 2048) >> 4);
-                                mma_ts(tmem + L::T_DV, tmem + L::T_S + half_packed_col(kk), dod_mn + step, L::ID_DKV,
-                                       (i > 0 || kk > 0) ? 1u : 0u);
-                            }
-                            tc_commit(bar(L::B_DVDONE));
-                            dv_done = progress = true;
-                        }
-                        if (!progress && !poll_continue(pc, ctx, SITE_M_DPDV)) {
-                            ok = false;
-                            break;
-                        }
-                    }
-                    if (!ok)
+                    // dP^T(g) = V_j dO^T, once dO(g) has landed (BULK: its own buffer) and, for
+                    // d = 128, into the columns of dQ^T(g-1) after its drain has read them
+                    if ((L::BULK && !wait(bar(L::B_DOFULL), g & 1, SITE_M_DPDV)) ||
+                        (L::DQ_ALIAS && g > 0 && !wait(bar(L::B_DQEMPTY), (g - 1) & 1, SITE_M_DQEMPTY))) {
+                        ok = false;
                         break;
-                    if constexpr (L::BULK)
-                        tc_commit(bar(L::B_DOEMPTY));   // dO(g) free once dP(g) and dV(g) complete
+                    }
+                    tc_fence_after();
+                    if (lane == 0) {
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint64_t ka = (uint64_t)(((kk >> 2) * L::KV_CHUNK + (kk & 3) * 32) >> 4);
+                            const uint64_t qa = (uint64_t)(((kk >> 2) * L::Q_CHUNK + (kk & 3) * 32) >> 4);
+                            mma_ss(tmem + L::T_DP, vd_k + ka, dod_k + qa, L::ID_SDP, kk > 0 ? 1u : 0u);
+                        }
+                        tc_commit(bar(L::B_DPFULL));
+                    }
+                    // dV_j += P^T dO after the softmax's P phase; the first block of a unit
+                    // overwrites the accumulator, after the previous unit's epilogue has read it
+                    if (!wait(bar(L::B_PFULL), g & 1, SITE_M_DPDV) ||
+                        (i == 0 && nu > 0 && !wait(bar(L::B_DKVEMPTY), (nu - 1) & 1, SITE_M_DPDV))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (lane == 0) {
+#pragma unroll
+                        for (int kk = 0; kk < BQ / 16; ++kk) {
+                            const uint64_t step = (uint64_t)((kk * 2048) >> 4);
+                            mma_ts(tmem + L::T_DV, tmem + L::T_S + half_packed_col(kk), dod_mn + step, L::ID_DKV,
+                                   (i > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        tc_commit(bar(L::B_DVDONE));
+                        if constexpr (L::BULK)
+                            tc_commit(bar(L::B_DOEMPTY));   // dO(g) free: dP(g) and dV(g) complete
+                    }
                     // S of the next block as soon as dV(g) has read P^T from its columns, so that
                     // the next P phase can follow this dS phase; then, once dS(g) is in shared
                     // memory, dQ and dK
@@ -500,13 +502,12 @@ __global__ void __launch_bounds__(512, 1)
                         ok = false;
                         break;
                     }
-                    if (!mbar_wait<true>(bar(L::B_DSFULL), g & 1, ctx, SITE_M_DSFULL)) {
+                    if (!wait(bar(L::B_DSFULL), g & 1, SITE_M_DSFULL)) {
                         ok = false;
                         break;
                     }
                     const uint32_t b = L::DQ_ALIAS ? 0u : (g & 1u);
-                    if (!L::DQ_ALIAS && g >= 2 &&
-                        !mbar_wait<true>(bar(L::B_DQEMPTY + b), ((g - 2) >> 1) & 1, ctx, SITE_M_DQEMPTY)) {
+                    if (!L::DQ_ALIAS && g >= 2 && !wait(bar(L::B_DQEMPTY + b), ((g - 2) >> 1) & 1, SITE_M_DQEMPTY)) {
                         ok = false;
                         break;
                     }
@@ -514,32 +515,35 @@ __global__ void __launch_bounds__(512, 1)
                     const uint32_t ds = ds_addr(g);
                     const uint64_t dsd_mn = sdesc_sw128(ds, L::DS_CHUNK, 1024);
                     const uint64_t dsd_k = sdesc_sw128(ds, 16, 1024);
+                    if (lane == 0) {
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
-                        const uint64_t step = (uint64_t)((kk * 2048) >> 4);
-                        if constexpr (L::DQ_ALIAS)
-                            mma_ss(tmem + L::T_DQ, kd_mn + step, dsd_mn + step, L::ID_DQ, kk > 0 ? 1u : 0u);
-                        else
-                            mma_ss(tmem + L::T_DQ + b * L::DQ_COLS, dsd_mn + step, kd_mn + step, L::ID_DQ,
-                                   kk > 0 ? 1u : 0u);
-                    }
-                    tc_commit(bar(L::B_DQFULL + b));
-                    // dK_j += dS^T Q  (dS^T from shared memory, K-major; Q MN-major)
+                        for (int kk = 0; kk < BK / 16; ++kk) {
+                            const uint64_t step = (uint64_t)((kk * 2048) >> 4);
+                            if constexpr (L::DQ_ALIAS)
+                                mma_ss(tmem + L::T_DQ, kd_mn + step, dsd_mn + step, L::ID_DQ, kk > 0 ? 1u : 0u);
+                            else
+                                mma_ss(tmem + L::T_DQ + b * L::DQ_COLS, dsd_mn + step, kd_mn + step, L::ID_DQ,
+                                       kk > 0 ? 1u : 0u);
+                        }
+                        tc_commit(bar(L::B_DQFULL + b));
+                        // dK_j += dS^T Q  (dS^T from shared memory, K-major; Q MN-major)
 #pragma unroll
-                    for (int kk = 0; kk < BQ / 16; ++kk) {
-                        const uint64_t da = (uint64_t)(((kk >> 2) * L::DS_CHUNK + (kk & 3) * 32) >> 4);
-                        const uint64_t step = (uint64_t)((kk * 2048) >> 4);
-                        mma_ss(tmem + L::T_DK, dsd_k + da, qd_mn + step, L::ID_DKV, (i > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    tc_commit(bar(L::B_STEMPTY + g % NST));
-                    if (i == x.nq - 1) {
-                        tc_commit(bar(L::B_DKVFULL));
-                        tc_commit(bar(L::B_KVEMPTY));
+                        for (int kk = 0; kk < BQ / 16; ++kk) {
+                            const uint64_t da = (uint64_t)(((kk >> 2) * L::DS_CHUNK + (kk & 3) * 32) >> 4);
+                            const uint64_t step = (uint64_t)((kk * 2048) >> 4);
+                            mma_ss(tmem + L::T_DK, dsd_k + da, qd_mn + step, L::ID_DKV, (i > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        tc_commit(bar(L::B_STEMPTY + g % NST));
+                        if (i == x.nq - 1) {
+                            tc_commit(bar(L::B_DKVFULL));
+                            tc_commit(bar(L::B_KVEMPTY));
+                        }
                     }
                 }
                 ++nu;
             }
-            tc_commit(bar(L::B_DRAIN));
+            if (lane == 0)
+                tc_commit(bar(L::B_DRAIN));
             mbar_wait_drain(bar(L::B_DRAIN), 0, a.timeout_ns);
         } else if (warp == 2 && lane == 0) {
             // -------------------------------------------------------- lse / D loader

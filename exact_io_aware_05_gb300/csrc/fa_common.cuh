@@ -74,20 +74,6 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok;
 }
 
-// Non-blocking probe of the phase with parity `parity` (no suspend hint).
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
 // Per-CTA context of the bounded waits: a shared abort flag that every role
 // polls, the kernel's device status word and the time limit.
 struct WaitCtx {
@@ -120,34 +106,6 @@ __device__ __forceinline__ bool mbar_wait_loop(uint32_t bar, uint32_t parity, co
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitCtx &ctx, int site)
 {
     return mbar_wait_loop(bar, parity, ctx, site);
-}
-
-// Bookkeeping of a hand-written polling loop that waits on several barriers at
-// once: call once per pass that made no progress.  Returns false when the loop
-// must give up: the abort flag is up, or ctx.timeout_ns has passed since the
-// first pass (then the abort flag is raised and the site recorded, as in
-// mbar_wait_slow).
-struct PollClock {
-    uint64_t t0 = 0;
-    uint32_t it = 0;
-};
-
-__device__ __forceinline__ bool poll_continue(PollClock &pc, const WaitCtx &ctx, int site)
-{
-    if (*ctx.abort)
-        return false;
-    if ((++pc.it & 31u) == 0u) {
-        const uint64_t now = globaltimer_ns();
-        if (pc.t0 == 0) {
-            pc.t0 = now;
-        } else if (now - pc.t0 > ctx.timeout_ns) {
-            *ctx.abort = 1;
-            atomicCAS(ctx.status, 0, (site << 8) | kStatusTimeout);
-            __threadfence();
-            return false;
-        }
-    }
-    return true;
 }
 
 // kInline: the slow path inlined instead of called.  Code that runs under a
