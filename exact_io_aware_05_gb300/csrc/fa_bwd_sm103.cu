@@ -896,8 +896,9 @@ __global__ void __launch_bounds__(256) bwd_kvmax_kernel(const __nv_bfloat16 *__r
 // -D_r = -(dO_r . O_r) and -lse_r in log2 units (-inf where no key is allowed or
 // past Tq), stored negated so that the tile loop adds them; the fp32 dQ
 // accumulator zeroed; deterministic mode: the fixed-point bound of each query
-// block, max over its rows of 2 |dO_r|_2 max|V|_2 max|K|.  One warp per
-// (padded) row.
+// block, max over its rows of 2 |dO_r|_2 max|V|_2 max|K|.  A group of D/8 lanes
+// takes a (padded) row, 16 bytes of O and of dO per lane, and every group keeps
+// two rows in flight so that enough loads are outstanding to stream HBM.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__restrict__ o,
                                                       const __nv_bfloat16 *__restrict__ dO,
@@ -906,60 +907,67 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__res
                                                       const float *__restrict__ kvmax, int *__restrict__ bound, int BH,
                                                       int Tq, int Tq_pad)
 {
+    constexpr int G = D / 8;        // lanes per row
+    constexpr int RPW = 32 / G;     // rows per warp and pass
+    constexpr int U = 2;            // passes in flight
     const size_t rows = (size_t)BH * Tq_pad;
-    const int lane = threadIdx.x & 31;
-    for (size_t gr = (blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5; gr < rows;
-         gr += ((size_t)gridDim.x * blockDim.x) >> 5) {
-        const size_t bh = gr / Tq_pad;
-        const int r = (int)(gr - bh * Tq_pad);
-        float dsum = 0.f, ss = 0.f;
-        if (r < Tq) {
-            const size_t src = (bh * Tq + r) * D;
-            constexpr int PER = D / 32;   // elements per lane (2 or 4)
-            if constexpr (PER == 4) {
-                const uint2 ov = *reinterpret_cast<const uint2 *>(o + src + lane * 4);
-                const uint2 gv = *reinterpret_cast<const uint2 *>(dO + src + lane * 4);
-                const __nv_bfloat162 *o2 = reinterpret_cast<const __nv_bfloat162 *>(&ov);
-                const __nv_bfloat162 *g2 = reinterpret_cast<const __nv_bfloat162 *>(&gv);
+    const int lane = threadIdx.x & 31, gi = lane / G, sub = lane % G;
+    const size_t warp = (blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5;
+    const size_t nwarps = ((size_t)gridDim.x * blockDim.x) >> 5;
+    // the loop is warp-uniform (whole warps take U * RPW rows), so the shuffles see all lanes
+    for (size_t wb = warp * (RPW * U); wb < rows; wb += nwarps * (RPW * U)) {
+        uint4 ov[U], gv[U];
+        size_t gr[U], bh[U];
+        int r[U];
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const float2 a2 = __bfloat1622float2(o2[e]), b2 = __bfloat1622float2(g2[e]);
-                    dsum = fmaf(a2.x, b2.x, dsum);
-                    dsum = fmaf(a2.y, b2.y, dsum);
-                    ss = fmaf(b2.x, b2.x, ss);
-                    ss = fmaf(b2.y, b2.y, ss);
-                }
-            } else {
-                const __nv_bfloat162 ov = *reinterpret_cast<const __nv_bfloat162 *>(o + src + lane * 2);
-                const __nv_bfloat162 gv = *reinterpret_cast<const __nv_bfloat162 *>(dO + src + lane * 2);
-                const float2 a2 = __bfloat1622float2(ov), b2 = __bfloat1622float2(gv);
+        for (int k = 0; k < U; ++k) {
+            gr[k] = wb + (size_t)k * RPW + gi;
+            bh[k] = gr[k] / Tq_pad;
+            r[k] = (int)(gr[k] - bh[k] * Tq_pad);
+            ov[k] = gv[k] = make_uint4(0u, 0u, 0u, 0u);
+            if (gr[k] < rows && r[k] < Tq) {
+                const size_t src = (bh[k] * Tq + r[k]) * D + sub * 8;
+                ov[k] = *reinterpret_cast<const uint4 *>(o + src);
+                gv[k] = *reinterpret_cast<const uint4 *>(dO + src);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            float dsum = 0.f, ss = 0.f;
+            const __nv_bfloat162 *o2 = reinterpret_cast<const __nv_bfloat162 *>(&ov[k]);
+            const __nv_bfloat162 *g2 = reinterpret_cast<const __nv_bfloat162 *>(&gv[k]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 a2 = __bfloat1622float2(o2[e]), b2 = __bfloat1622float2(g2[e]);
                 dsum = fmaf(a2.x, b2.x, dsum);
                 dsum = fmaf(a2.y, b2.y, dsum);
                 ss = fmaf(b2.x, b2.x, ss);
                 ss = fmaf(b2.y, b2.y, ss);
             }
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
+            for (int off = G / 2; off > 0; off >>= 1) {
                 dsum += __shfl_xor_sync(0xffffffffu, dsum, off);
                 ss += __shfl_xor_sync(0xffffffffu, ss, off);
             }
-        }
-        if (lane == 0) {
-            float l2 = -INFINITY;
-            if (r < Tq) {
-                const float lv = lse[bh * Tq + r];
-                l2 = (lv == -INFINITY) ? -INFINITY : -lv * 1.4426950408889634f;
+            if (gr[k] >= rows)
+                continue;
+            if (sub == 0) {
+                float l2 = -INFINITY;
+                if (r[k] < Tq) {
+                    const float lv = lse[bh[k] * Tq + r[k]];
+                    l2 = (lv == -INFINITY) ? -INFINITY : -lv * 1.4426950408889634f;
+                }
+                lse2[gr[k]] = l2;
+                delta[gr[k]] = r[k] < Tq ? -dsum : 0.f;
+                if (bound && r[k] < Tq) {
+                    const float bnd = 2.f * sqrtf(ss) * kvmax[2 * bh[k]] * kvmax[2 * bh[k] + 1];
+                    atomicMax(bound + (gr[k] >> 7), __float_as_int(bnd));
+                }
             }
-            lse2[gr] = l2;
-            delta[gr] = r < Tq ? -dsum : 0.f;
-            if (bound && r < Tq) {
-                const float bnd = 2.f * sqrtf(ss) * kvmax[2 * bh] * kvmax[2 * bh + 1];
-                atomicMax(bound + (gr >> 7), __float_as_int(bnd));
-            }
+            float4 *z = reinterpret_cast<float4 *>(dq_acc + gr[k] * D) + sub * 2;
+            z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+            z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        float4 *z = reinterpret_cast<float4 *>(dq_acc + gr * D);
-        for (int e = lane; e < D / 4; e += 32)
-            z[e] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
 }
 
@@ -1021,8 +1029,9 @@ int launch_bwd(const void *q, const void *k, const void *v, const void *o, const
                     return ERR_CUDA;
             }
         }
-        const size_t blocks = (rows + 7) / 8;
-        const int grid = (int)(blocks < (size_t)sms * 16 ? blocks : (size_t)sms * 16);
+        const size_t rows_per_block = 8 * (32 / (D / 8)) * 2;   // 8 warps x rows per warp x passes in flight
+        const size_t blocks = (rows + rows_per_block - 1) / rows_per_block;
+        const int grid = (int)(blocks < (size_t)sms * 8 ? blocks : (size_t)sms * 8);
         bwd_pre_kernel<D><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(o),
                                                static_cast<const __nv_bfloat16 *>(dO), lse, ws.lse2, ws.delta,
                                                ws.dq_acc, ws.kvmax, det ? ws.bound : nullptr, BH, Tq, Tq_pad);
