@@ -7,7 +7,7 @@
 //                dV_j += P_ij^T dO_i,  dP_ij = dO_i V_j^T,  dS_ij = P_ij o (dP_ij - D_i)
 //                dK_j += c dS_ij^T Q_i,  dQ_i += c dS_ij K_j      (observation 3)
 // with the key blocks outside: dK_j and dV_j accumulate on chip and are
-// written once, dQ_i is accumulated in HBM by fp32 atomic additions ("Which
+// written once, dQ_i is accumulated in HBM by fp32 reduce-additions ("Which
 // loop goes outside?").  Causal tiles wholly above the diagonal are skipped,
 // exactly as in the forward pass.  Five tile products per tile ("The price of
 // recomputation").
@@ -57,7 +57,7 @@ struct BwdLayout {
     static constexpr int Q_TILE = KCH * Q_CHUNK;
     // d = 128: dQ^T leaves through shared memory as bulk reduce-adds (TMA), staged in two
     // 16 KB buffers; to make room, dO has one buffer of its own and only Q is staged
-    // ahead.  d = 64: Q and dO share each stage, dQ leaves by atomic adds.
+    // ahead.  d = 64: Q and dO share each stage; each drain warp stages its own dQ rows.
     static constexpr bool BULK = DQ_ALIAS;
     static constexpr int NST = D == 128 ? 2 : 3;          // Q (and dO) stages
     static constexpr int ST_Q = 0, ST_DO = BULK ? 0 : Q_TILE, ST_BYTES = BULK ? Q_TILE : 2 * Q_TILE;
