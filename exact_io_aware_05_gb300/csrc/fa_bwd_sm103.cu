@@ -16,8 +16,9 @@
 //   * three kernels on one stream: bwd_pre (-D, -lse in log2 units, dQ
 //     accumulator zeroed), bwd_main (the tile loop below), bwd_dq (scale and
 //     round dQ);
-//   * bwd_main is persistent; a unit is one 128-key block of one head, taken
-//     longest-first within groups of heads; query blocks are 128 rows, so every
+//   * bwd_main is persistent; a unit is one 128-key block of one head; units are
+//     ordered longest-first within groups of heads and dealt to the CTAs in snake
+//     order (passes alternate direction); query blocks are 128 rows, so every
 //     product is a full M128 x N128 (d = 128) tensor-core instruction;
 //   * warp 0 streams K_j, V_j once per unit and Q_i, dO_i per query block
 //     through a ring of stages (TMA); warp 1 issues all tcgen05.mma; warp 2
@@ -356,7 +357,7 @@ __global__ void __launch_bounds__(512, 1)
             const uint64_t pol_keep = policy_evict_last();
             uint32_t n_kv = 0, n_st = 0;   // BULK: n_st also counts dO loads (one per block)
             bool ok = true;
-            for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+            for (int pass = 0, u = snake_unit<!MASKED>(0); u < a.units && ok; u = snake_unit<!MASKED>(++pass)) {
                 const Unit x = make_unit<MASKED>(u, a);
                 if (x.nq == 0)
                     continue;
@@ -447,7 +448,7 @@ __global__ void __launch_bounds__(512, 1)
                 }
                 return true;
             };
-            for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+            for (int pass = 0, u = snake_unit<!MASKED>(0); u < a.units && ok; u = snake_unit<!MASKED>(++pass)) {
                 const Unit x = make_unit<MASKED>(u, a);
                 if (x.nq == 0)
                     continue;
@@ -551,7 +552,7 @@ __global__ void __launch_bounds__(512, 1)
             // done, -D of block g once its dS phase is done.
             uint32_t g = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+            for (int pass = 0, u = snake_unit<!MASKED>(0); u < a.units && ok; u = snake_unit<!MASKED>(++pass)) {
                 const Unit x = make_unit<MASKED>(u, a);
                 for (int i = 0, qi = x.i0; i < x.nq; ++i, ++g, qi = MASKED ? unit_next(x, qi + 1, a.nkbm) : qi + 1) {
                     const size_t roff = (size_t)x.bh * a.Tq_pad + (size_t)qi * BQ;
@@ -585,7 +586,7 @@ __global__ void __launch_bounds__(512, 1)
         const float sl2 = a.scale_log2;
         uint32_t g = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+        for (int pass = 0, u = snake_unit<!MASKED>(0); u < a.units && ok; u = snake_unit<!MASKED>(++pass)) {
             const Unit x = make_unit<MASKED>(u, a);
             const int l = x.j * BK + key_in_blk;         // this thread's key
             for (int i = 0, qi = x.i0; i < x.nq; ++i, ++g, qi = MASKED ? unit_next(x, qi + 1, a.nkbm) : qi + 1) {
@@ -688,7 +689,7 @@ __global__ void __launch_bounds__(512, 1)
         uint32_t stg_n = 0;                          // dQ chunks staged so far (BULK)
         const bool lead = warp == 12 && lane == 0;   // issues the bulk reduce-adds
         bool ok = true;
-        for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+        for (int pass = 0, u = snake_unit<!MASKED>(0); u < a.units && ok; u = snake_unit<!MASKED>(++pass)) {
             const Unit x = make_unit<MASKED>(u, a);
             const int l = x.j * BK + row;
             const size_t krow = (size_t)x.bh * a.Tk + l;
@@ -1066,9 +1067,14 @@ int launch_bwd(const void *q, const void *k, const void *v, const void *o, const
         a.scale_log2 = scale * 1.4426950408889634f;
         a.nkb = (Tk + BK - 1) / BK;
         a.units = BH * a.nkb;
-        const double bytes_head = 2.0 * (Tq + Tk) * D * 2.0;   // Q, dO, K, V of one head
-        int gsz = (int)(48.0 * 1024 * 1024 / (bytes_head > 1 ? bytes_head : 1));
-        a.group = gsz < 1 ? 1 : (gsz > BH ? BH : gsz);
+        // heads per group: Q, dO, K, V of the group within ~80 MB of L2, a whole number of
+        // passes where possible (B8 H32 N4096 d128: 19 heads; measured faster than 12).  The
+        // masked instance keeps ~48 MB groups and same-direction passes (measured faster
+        // there: its units' lengths do not follow the order).
+        const double bytes_head = 2.0 * (Tq + Tk) * D * 2.0;
+        int gsz = (int)((masked ? 48.0 : 80.0) * 1024 * 1024 / (bytes_head > 1 ? bytes_head : 1));
+        gsz = gsz < 1 ? 1 : (gsz > BH ? BH : gsz);
+        a.group = masked ? gsz : grid_aligned_group(gsz, a.nkb, a.units < sms ? a.units : sms);
         a.timeout_ns = wait_timeout_ns();
         a.det_bound = det ? ws.bound : nullptr;
         a.left = mask.left;

@@ -74,6 +74,18 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok;
 }
 
+// Unit of pass k of this CTA in a persistent loop over units.  SNAKE: passes
+// alternate direction, so that with units sorted longest-first inside a group
+// each CTA takes long and short units alike; otherwise every pass runs the same
+// way.  The sequence increases with k, so a loop ends at the first unit past the
+// end.
+template <bool SNAKE>
+__device__ __forceinline__ int snake_unit(int k)
+{
+    const int c = (SNAKE && (k & 1)) ? (int)gridDim.x - 1 - (int)blockIdx.x : (int)blockIdx.x;
+    return k * (int)gridDim.x + c;
+}
+
 // Per-CTA context of the bounded waits: a shared abort flag that every role
 // polls, the kernel's device status word and the time limit.
 struct WaitCtx {

@@ -17,8 +17,9 @@
 //
 // GB300 design (differs from the pages' A100/H100 kernels):
 //   * persistent CTAs, one per SM, each owning a 256-row unit (two 128-row
-//     query tiles, d = 64/128) or a 128-row unit (d = 256); units are taken
-//     longest-first within groups of heads sized so their K/V stay in L2;
+//     query tiles, d = 64/128) or a 128-row unit (d = 256); units are ordered
+//     longest-first within groups of heads sized so their K/V stay in L2, and
+//     dealt to the CTAs in snake order (passes alternate direction);
 //   * warp 0: TMA producer (Q once per unit, K/V tiles through an NSLOT-deep
 //     ring with full/empty mbarriers);
 //   * warps 1 and 2 (two tiles): one thread each issues the tcgen05.mma and
@@ -421,7 +422,7 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
             if (lane == 0) {
                 const uint64_t pol_kv = policy_evict_last();
                 const uint64_t pol_q = policy_evict_first();
-                for (int u = blockIdx.x; u < a.units; u += gridDim.x) {
+                for (int pass = 0, u = snake_unit<!MASKED>(0); u < a.units; u = snake_unit<!MASKED>(++pass)) {
                     const Plan p = make_plan<D, MASKED>(u, a);
                     if (p.J == 0)
                         continue;
@@ -511,7 +512,7 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                 const uint32_t drain_bar = bar(t == 0 ? L::B_DRAIN : L::B_DRAIN1);
                 uint32_t ld = 0, q_seen = 0, sn = 0, pvn = 0, epi = 0;
                 bool ok = true;
-                for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+                for (int pass = 0, u = snake_unit<!MASKED>(0); u < a.units && ok; u = snake_unit<!MASKED>(++pass)) {
                     const Plan p = make_plan<D, MASKED>(u, a);
                     if (p.J == 0)
                         continue;
@@ -616,7 +617,7 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
             if (lane == 0) {
                 uint32_t ld = 0, kg = 0, q_seen = 0;
                 uint32_t epi[2] = {0, 0};
-                for (int u = blockIdx.x; u < a.units; u += gridDim.x) {
+                for (int pass = 0, u = snake_unit<!MASKED>(0); u < a.units; u = snake_unit<!MASKED>(++pass)) {
                     const Plan p = make_plan<D, MASKED>(u, a);
                     if (p.J == 0)
                         continue;
@@ -716,7 +717,7 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
         const uint32_t lane_base = tmem + ((quarter * 32u) << 16);
         uint32_t pv = 0, ep = 0;   // jobs and epilogues of this tile so far
         // The two softmax warpgroups run unsynchronised: each follows its own tile's S.
-        for (int u = blockIdx.x; u < a.units; u += gridDim.x) {
+        for (int pass = 0, u = snake_unit<!MASKED>(0); u < a.units; u = snake_unit<!MASKED>(++pass)) {
             const Plan p = make_plan<D, MASKED>(u, a);
             const int r = p.row0 + t * BR + rit;
             const TileRange me = tile_of(p, t);
@@ -1023,12 +1024,16 @@ int launch(const void *q, const void *k, const void *v, void *o, float *lse, int
     a.nqd = a.nkd = 0;
     a.nqb = (Tq + L::NQ * BR - 1) / (L::NQ * BR);
     a.units = BH * a.nqb;
-    // heads per group: keep the group's K and V within ~48 MB of L2
+    // heads per group: keep the group's K and V within ~80 MB of L2, a whole number of
+    // passes where possible (B8 H32 N4096 d128: 38 heads; measured faster than 24).  The
+    // masked instance keeps ~48 MB groups and same-direction passes: its units' lengths
+    // do not follow the order, and there the smaller groups measured faster.
     const double kv_head = 2.0 * Tk * D * 2.0;
-    int g = (int)(48.0 * 1024 * 1024 / (kv_head > 1 ? kv_head : 1));
-    a.group = g < 1 ? 1 : (g > BH ? BH : g);
-    a.timeout_ns = wait_timeout_ns();
     const int grid = a.units < device_sm_count() ? a.units : device_sm_count();
+    int g = (int)((a.masked ? 48.0 : 80.0) * 1024 * 1024 / (kv_head > 1 ? kv_head : 1));
+    g = g < 1 ? 1 : (g > BH ? BH : g);
+    a.group = a.masked ? g : grid_aligned_group(g, a.nqb, grid);
+    a.timeout_ns = wait_timeout_ns();
     auto kernel = a.masked ? fwd_kernel<D, true> : fwd_kernel<D, false>;
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES) != cudaSuccess)
         return ERR_CUDA;
@@ -1073,11 +1078,12 @@ int launch_f8(const void *q8, const void *k8, const void *vt8, const float *qd, 
     a.nkd = (Tk + 127) / 128;
     a.nqb = (Tq + L::NQ * BR - 1) / (L::NQ * BR);
     a.units = BH * a.nqb;
+    // heads per group: K and V (e4m3) within ~48 MB of L2, which measured faster than 80 MB here
     const double kv_head = 2.0 * Tk * D;
     int g = (int)(48.0 * 1024 * 1024 / (kv_head > 1 ? kv_head : 1));
-    a.group = g < 1 ? 1 : (g > BH ? BH : g);
-    a.timeout_ns = wait_timeout_ns();
     const int grid = a.units < device_sm_count() ? a.units : device_sm_count();
+    a.group = grid_aligned_group(g < 1 ? 1 : (g > BH ? BH : g), a.nqb, grid);
+    a.timeout_ns = wait_timeout_ns();
     auto kernel = fwd_kernel<D, false, true>;
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES) != cudaSuccess)
         return ERR_CUDA;

@@ -21,6 +21,19 @@ int encode_tmap_3d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype
 
 int device_sm_count();          // SMs of the current device (cached per device)
 uint64_t wait_timeout_ns();     // bounded-wait limit for device spin waits
+// Heads per group of a persistent kernel's unit order.  gmax keeps the group's
+// tensors within the L2 budget; where a group size in [gmax/2, gmax] makes a group
+// a whole number of passes over the grid (levels units per head), the snake order
+// of the passes balances the CTAs, so that size is taken.
+inline int grid_aligned_group(int gmax, int levels, int grid)
+{
+    if (gmax < 1)
+        gmax = 1;
+    for (int g = gmax; g >= 1 && 2 * g >= gmax; --g)
+        if (grid > 0 && ((long long)g * levels) % grid == 0)
+            return g;
+    return gmax;
+}
 
 // Allowed (row, key) pairs: key l is allowed for row r iff
 //   r + Tk - Tq - left <= l <= r + Tk - Tq + right   (left, right = -1: that side unbounded)
