@@ -90,6 +90,23 @@ uint64_t wait_timeout_ns()
     return ns;
 }
 
+#if FA_TEST_WITHHOLD
+namespace {
+std::mutex g_withhold_mu;
+int g_withhold = WITHHOLD_NONE;
+}  // namespace
+
+int test_withhold_take(int lo, int hi)
+{
+    std::lock_guard<std::mutex> lock(g_withhold_mu);
+    const int w = g_withhold;
+    if (w < lo || w > hi)
+        return WITHHOLD_NONE;
+    g_withhold = WITHHOLD_NONE;
+    return w;
+}
+#endif
+
 // ------------------------------------------------------------ fill kernel
 // Rows with no key at all (Tk == 0): O = 0, lse = -inf.
 __global__ void fill_empty_kernel(uint8_t *o, float *lse, size_t rows, int row_bytes)
@@ -187,9 +204,9 @@ size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 size_t bwd_row_stride(int Tq) { return ((size_t)Tq + 127) / 128 * 128; }
 
-size_t bwd_workspace_bytes(int BH, int Tq, int d)
+size_t bwd_workspace_bytes(size_t BH, int Tq, int d)
 {
-    const size_t rows = (size_t)BH * bwd_row_stride(Tq);
+    const size_t rows = BH * bwd_row_stride(Tq);
     return 2 * round256(rows * sizeof(float)) + round256(rows * d * sizeof(float)) +
            round256((size_t)BH * 2 * sizeof(float) + rows / 128 * sizeof(int));
 }
@@ -206,6 +223,48 @@ BwdWorkspace bwd_workspace_carve(void *ws, int BH, int Tq, int d)
     w.kvmax = reinterpret_cast<float *>(det);
     w.bound = reinterpret_cast<int *>(det + (size_t)BH * 2 * sizeof(float));
     return w;
+}
+
+
+// Every check of the backward's arguments except those of the workspace and the device:
+// sizes, flags, scale, head width, and the tensors' presence, alignment and overlaps.
+// Makes no CUDA call.  OK also when there is nothing to compute.
+int bwd_check_args(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dO,
+                   const void *dq, const void *dk, const void *dv, int B, int H, int Tq, int Tk, int d,
+                   const MaskSpec &mask, float scale)
+{
+    int st = check_sizes(B, H, Tq, Tk, d, 0, scale);
+    if (st != OK)
+        return st;
+    if (mask.left < -1 || mask.right < -1 || mask.per_head < 0 || mask.per_head > 1)
+        return ERR_INVALID_ARG;
+    if (d == 256)
+        return ERR_UNSUPPORTED;
+    const size_t bh = (size_t)B * H;
+    if (bh == 0 || (Tq == 0 && Tk == 0))
+        return OK;
+    const size_t nq = bh * Tq * d * 2, nk = bh * Tk * d * 2, nl = bh * Tq * sizeof(float);
+    if ((Tq > 0 && (!q || !o || !lse || !dO || !dq)) || (Tk > 0 && (!k || !v || !dk || !dv)))
+        return ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dO) ||
+        !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+        return ERR_INVALID_ARG;
+    const void *ins[6] = {q, k, v, o, lse, dO};
+    const size_t in_n[6] = {nq, nk, nk, nq, nl, nq};
+    const void *outs[3] = {dq, dk, dv};
+    const size_t out_n[3] = {nq, nk, nk};
+    const size_t nm = (mask.per_head ? bh : 1) * (size_t)((Tq + 127) / 128) * ((Tk + 127) / 128);
+    for (int i = 0; i < 3; ++i) {
+        for (int j = 0; j < 6; ++j)
+            if (overlaps(outs[i], out_n[i], ins[j], in_n[j]))
+                return ERR_INVALID_ARG;
+        for (int j = i + 1; j < 3; ++j)
+            if (overlaps(outs[i], out_n[i], outs[j], out_n[j]))
+                return ERR_INVALID_ARG;
+        if (mask.block && overlaps(outs[i], out_n[i], mask.block, nm))
+            return ERR_INVALID_ARG;
+    }
+    return OK;
 }
 
 }  // namespace fa
@@ -380,31 +439,27 @@ size_t fa_bwd_workspace_bytes(int B, int H, int Tq, int Tk, int d)
 {
     if (B < 0 || H < 0 || Tq < 0 || Tk < 0 || (d != 64 && d != 128 && d != 256))
         return 0;
-    return fa::bwd_workspace_bytes(B * H, Tq, d);
+    if ((long long)B * H > INT_MAX)   // the kernels index heads with 32-bit integers
+        return 0;
+    return fa::bwd_workspace_bytes((size_t)B * H, Tq, d);
 }
+
 
 static int bwd_common(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dO,
                       void *dq, void *dk, void *dv, int B, int H, int Tq, int Tk, int d, const fa::MaskSpec &mask,
                       float scale, void *workspace, size_t workspace_bytes, int stages, fa_stream_t stream)
 {
-    int st = fa::check_sizes(B, H, Tq, Tk, d, 0, scale);
+    int st = fa::bwd_check_args(q, k, v, o, lse, dO, dq, dk, dv, B, H, Tq, Tk, d, mask, scale);
     if (st != fa::OK)
         return st;
-    if (mask.left < -1 || mask.right < -1 || mask.per_head < 0 || mask.per_head > 1)
-        return FA_ERR_INVALID_ARG;
-    if (d == 256)
-        return FA_ERR_UNSUPPORTED;
     const size_t bh = (size_t)B * H;
     if (bh == 0 || (Tq == 0 && Tk == 0))
         return FA_OK;
     const size_t nq = bh * Tq * d * 2, nk = bh * Tk * d * 2, nl = bh * Tq * sizeof(float);
-    const size_t need = fa::bwd_workspace_bytes((int)bh, Tq, d);
-    if ((Tq > 0 && (!q || !o || !lse || !dO || !dq)) || (Tk > 0 && (!k || !v || !dk || !dv)) ||
-        (need > 0 && (!workspace || workspace_bytes < need)))
+    const size_t need = fa::bwd_workspace_bytes(bh, Tq, d);
+    if (need > 0 && (!workspace || workspace_bytes < need))
         return FA_ERR_INVALID_ARG;
-    if (!fa::aligned16(q) || !fa::aligned16(k) || !fa::aligned16(v) || !fa::aligned16(o) || !fa::aligned16(lse) ||
-        !fa::aligned16(dO) || !fa::aligned16(dq) || !fa::aligned16(dk) || !fa::aligned16(dv) ||
-        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return FA_ERR_INVALID_ARG;
     const void *ins[6] = {q, k, v, o, lse, dO};
     const size_t in_n[6] = {nq, nk, nk, nq, nl, nq};
@@ -505,5 +560,27 @@ const char *fa_status_string(int status)
         return "unknown status";
     }
 }
+
+#if FA_TEST_WITHHOLD
+// Test-only exports (absent from the product library): arm one withheld arrive for the
+// next matching launch, and read the raw status word (wait site << 8 | status).
+void fa_test_withhold(int which)
+{
+    std::lock_guard<std::mutex> lock(fa::g_withhold_mu);
+    fa::g_withhold = which;
+}
+
+int fa_test_status_word(fa_stream_t stream)
+{
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess)
+        return -1;
+    int wf = 0, wb = 0, wd = 0;
+    if (fa::fwd_status_fetch_clear(s, &wf) != fa::OK || fa::bwd_status_fetch_clear(s, &wb) != fa::OK ||
+        fa::dec_status_fetch_clear(s, &wd) != fa::OK)
+        return -1;
+    return wf ? wf : (wb ? wb : wd);
+}
+#endif
 
 }  // extern "C"

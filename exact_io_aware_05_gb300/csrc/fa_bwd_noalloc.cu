@@ -13,8 +13,10 @@
 // until the process exits (with CUDA's default lazy module loading, that is
 // from the first call of fa_bwd_noalloc on that device).  In host code the
 // array's name is only a host-side stand-in, so its device address is looked
-// up once per device with cudaGetSymbolAddress, with that device current,
-// and cached.
+// up with cudaGetSymbolAddress, with the device current, and cached per device
+// together with the CUDA context it belongs to: a call under another context
+// (after cudaDeviceReset, or a context the caller made current) looks it up
+// again instead of using an address of a context that no longer holds it.
 #include <mutex>
 
 #include "../../include/fa.h"
@@ -26,10 +28,30 @@ static __device__ __align__(256) unsigned char g_bwd_noalloc_scratch[FA_BWD_NOAL
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-void *g_scratch_addr[kMaxDevices] = {nullptr};
+struct Cached {
+    CUcontext ctx;
+    void *addr;
+};
+Cached g_scratch[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device; looked up on the
-// first call for that device.
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+
+CtxGetCurrentFn ctx_get_current()
+{
+    static std::once_flag once;
+    static CtxGetCurrentFn fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(p);
+    });
+    return fn;
+}
+
+// Device address of the scratch array in the current device's current context;
+// looked up on the first call for that (device, context).
 int scratch_address(void **out)
 {
     int dev = 0;
@@ -37,14 +59,24 @@ int scratch_address(void **out)
         return FA_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices)
         return FA_ERR_UNSUPPORTED;
+    CtxGetCurrentFn get = ctx_get_current();
+    if (!get)
+        return FA_ERR_CUDA;
+    // With no context current yet, cudaGetSymbolAddress below makes the device's primary
+    // context current; the context is read again after it.
+    CUcontext ctx = nullptr;
+    if (get(&ctx) != CUDA_SUCCESS)
+        return FA_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_scratch_addr[dev]) {
+    if (!g_scratch[dev].addr || !ctx || g_scratch[dev].ctx != ctx) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_bwd_noalloc_scratch) != cudaSuccess || p == nullptr)
             return FA_ERR_CUDA;
-        g_scratch_addr[dev] = p;
+        if (get(&ctx) != CUDA_SUCCESS || !ctx)
+            return FA_ERR_CUDA;
+        g_scratch[dev] = Cached{ctx, p};
     }
-    *out = g_scratch_addr[dev];
+    *out = g_scratch[dev].addr;
     return FA_OK;
 }
 
@@ -54,13 +86,20 @@ extern "C" int fa_bwd_noalloc(const void *q, const void *k, const void *v, const
                               const void *dO, void *dq, void *dk, void *dv, int B, int H, int Tq, int Tk, int d,
                               int causal, float scale, fa_stream_t stream)
 {
+    // fa_bwd's own argument errors first (no CUDA call), then the scratch limit
+    if (causal != 0 && causal != 1)
+        return FA_ERR_INVALID_ARG;
+    const int st = fa::bwd_check_args(q, k, v, o, lse, dO, dq, dk, dv, B, H, Tq, Tk, d, fa::causal_spec(causal),
+                                      scale);
+    if (st != FA_OK)
+        return st;
     const size_t need = fa_bwd_workspace_bytes(B, H, Tq, Tk, d);
     if (need > (size_t)FA_BWD_NOALLOC_SCRATCH_BYTES)
         return FA_ERR_UNSUPPORTED;
     void *scratch = nullptr;
-    const int st = scratch_address(&scratch);
-    if (st != FA_OK)
-        return st;
+    const int sa = scratch_address(&scratch);
+    if (sa != FA_OK)
+        return sa;
     return fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, Tq, Tk, d, causal, scale, scratch,
                   (size_t)FA_BWD_NOALLOC_SCRATCH_BYTES, stream);
 }

@@ -111,6 +111,7 @@ struct BwdArgs {
     float scale, scale_log2;
     int nkb, units, group;
     uint64_t timeout_ns;
+    int withhold;           // test-only build: the arrive this launch leaves out (else 0, unused)
     const int *det_bound;   // deterministic mode: per 128-row query block, bound on |dq_acc| (else null)
     // masked instance: allowed keys of row r are r + Tk - Tq - left .. r + Tk - Tq + right
     // (-1: unbounded side), in 128 x 128 blocks marked by bmask ([heads][nqbm][nkbm] or null)
@@ -355,7 +356,7 @@ __global__ void __launch_bounds__(512, 1)
         if (warp == 0 && lane == 0) {
             // -------------------------------------------------------- producer
             const uint64_t pol_keep = policy_evict_last();
-            uint32_t n_kv = 0, n_st = 0;   // BULK: n_st also counts dO loads (one per block)
+            uint32_t n_kv = 0, n_st = 0, n_do = 0;   // K/V, stage (Q, and dO unless BULK) and BULK dO loads issued
             bool ok = true;
             for (int pass = 0, u = snake_unit<!MASKED>(0); u < a.units && ok; u = snake_unit<!MASKED>(++pass)) {
                 const Unit x = make_unit<MASKED>(u, a);
@@ -384,10 +385,11 @@ __global__ void __launch_bounds__(512, 1)
                             tma_load_3d_hint(st + L::ST_DO + c * L::Q_CHUNK, &tm_do, bar(L::B_STFULL + s), c * 64,
                                              i * BQ, x.bh, pol_keep);
                     }
+                    ++n_st;   // counted as soon as issued: the drain below waits for every issued copy
                     if constexpr (L::BULK) {
-                        // dO of block n_st: its one buffer is free once dP and dV of the previous
+                        // dO of this block: its one buffer is free once dP and dV of the previous
                         // block, its readers, have completed
-                        if (n_st > 0 && !mbar_wait<true>(bar(L::B_DOEMPTY), (n_st - 1) & 1, ctx, SITE_P_STEMPTY)) {
+                        if (n_do > 0 && !mbar_wait<true>(bar(L::B_DOEMPTY), (n_do - 1) & 1, ctx, SITE_P_STEMPTY)) {
                             ok = false;
                             break;
                         }
@@ -395,18 +397,18 @@ __global__ void __launch_bounds__(512, 1)
                         for (int c = 0; c < L::KCH; ++c)
                             tma_load_3d_hint(sbase + L::OFF_DO + c * L::Q_CHUNK, &tm_do, bar(L::B_DOFULL), c * 64,
                                              i * BQ, x.bh, pol_keep);
+                        ++n_do;
                     }
-                    ++n_st;
                 }
             }
             // drain copies in flight
             const uint32_t lo = n_st > (uint32_t)NST ? n_st - NST : 0;
             for (uint32_t i = lo; i < n_st; ++i)
-                mbar_wait_drain(bar(L::B_STFULL + i % NST), (i / NST) & 1, a.timeout_ns);
-            if (L::BULK && n_st > 0)
-                mbar_wait_drain(bar(L::B_DOFULL), (n_st - 1) & 1, a.timeout_ns);
+                mbar_wait_drain(bar(L::B_STFULL + i % NST), (i / NST) & 1);
+            if (L::BULK && n_do > 0)
+                mbar_wait_drain(bar(L::B_DOFULL), (n_do - 1) & 1);
             if (n_kv > 0)
-                mbar_wait_drain(bar(L::B_KVFULL), (n_kv - 1) & 1, a.timeout_ns);
+                mbar_wait_drain(bar(L::B_KVFULL), (n_kv - 1) & 1);
         } else if (warp == 1) {
             // -------------------------------------------------------- MMA issuer
         // Per block g the tensor core runs dP(g) dV(g) S(g+1) dQ(g) dK(g): dP first (its inputs
@@ -536,7 +538,13 @@ __global__ void __launch_bounds__(512, 1)
                         }
                         tc_commit(bar(L::B_STEMPTY + g % NST));
                         if (i == x.nq - 1) {
-                            tc_commit(bar(L::B_DKVFULL));
+#if FA_TEST_WITHHOLD
+                            const bool hold = a.withhold == WITHHOLD_BWD_DKV && blockIdx.x == 0 && nu == 0;
+#else
+                            constexpr bool hold = false;
+#endif
+                            if (!hold)
+                                tc_commit(bar(L::B_DKVFULL));
                             tc_commit(bar(L::B_KVEMPTY));
                         }
                     }
@@ -545,7 +553,7 @@ __global__ void __launch_bounds__(512, 1)
             }
             if (lane == 0)
                 tc_commit(bar(L::B_DRAIN));
-            mbar_wait_drain(bar(L::B_DRAIN), 0, a.timeout_ns);
+            mbar_wait_drain(bar(L::B_DRAIN), 0);
         } else if (warp == 2 && lane == 0) {
             // -------------------------------------------------------- lse / D loader
             // One buffer each: -lse of block g is loaded once the P phase of block g-1 is
@@ -572,8 +580,8 @@ __global__ void __launch_bounds__(512, 1)
             }
             // copies in flight: the last phase of each buffer that was started
             if (g > 0) {
-                mbar_wait_drain(bar(L::B_LFULL), (g - 1) & 1, a.timeout_ns);
-                mbar_wait_drain(bar(L::B_DFULL), (g - 1) & 1, a.timeout_ns);
+                mbar_wait_drain(bar(L::B_LFULL), (g - 1) & 1);
+                mbar_wait_drain(bar(L::B_DFULL), (g - 1) & 1);
             }
         }
         __syncwarp();
@@ -605,8 +613,8 @@ __global__ void __launch_bounds__(512, 1)
                         qmax = (int)max(0L, min(64L, (long)l - off + a.left - qb + 1));
                 }
                 const bool mask = __any_sync(0xffffffffu, qmin > 0 || qmax < 64);
-                if (!mbar_wait(bar(L::B_SFULL), g & 1, ctx, SITE_S_SFULL) ||
-                    !mbar_wait(bar(L::B_LFULL), g & 1, ctx, SITE_S_LFULL)) {
+                if (!mbar_wait_warp(bar(L::B_SFULL), g & 1, ctx, SITE_S_SFULL) ||
+                    !mbar_wait_warp(bar(L::B_LFULL), g & 1, ctx, SITE_S_LFULL)) {
                     ok = false;
                     break;
                 }
@@ -641,8 +649,8 @@ __global__ void __launch_bounds__(512, 1)
                 mbar_arrive(bar(L::B_PFULL));
                 // dS phase: dS = P o (dP - D) into shared memory ([key][query], 128-byte
                 // swizzle, 64 queries per 128-byte row)
-                if (!mbar_wait(bar(L::B_DPFULL), g & 1, ctx, SITE_S_DPFULL) ||
-                    !mbar_wait(bar(L::B_DFULL), g & 1, ctx, SITE_S_DFULL)) {
+                if (!mbar_wait_warp(bar(L::B_DPFULL), g & 1, ctx, SITE_S_DPFULL) ||
+                    !mbar_wait_warp(bar(L::B_DFULL), g & 1, ctx, SITE_S_DFULL)) {
                     ok = false;
                     break;
                 }
@@ -710,6 +718,8 @@ __global__ void __launch_bounds__(512, 1)
                 bool got = mbar_wait<true>(bar(L::B_DQFULL + b), ph, ctx, SITE_D_DQFULL);
                 if constexpr (L::BULK)
                     got = drain_all(got);   // one decision for the warpgroup (named barriers follow)
+                else
+                    got = __all_sync(0xffffffffu, got);   // one decision for the warp (tensor-memory loads follow)
                 if (!got) {
                     ok = false;
                     break;
@@ -818,6 +828,8 @@ __global__ void __launch_bounds__(512, 1)
             bool kv_ok = mbar_wait<true>(bar(L::B_DKVFULL), nu & 1, ctx, SITE_D_DKVFULL);
             if constexpr (L::BULK)
                 kv_ok = drain_all(kv_ok);
+            else
+                kv_ok = __all_sync(0xffffffffu, kv_ok);
             if (!kv_ok)
                 break;
             tc_fence_after();
@@ -1076,6 +1088,10 @@ int launch_bwd(const void *q, const void *k, const void *v, const void *o, const
         gsz = gsz < 1 ? 1 : (gsz > BH ? BH : gsz);
         a.group = masked ? gsz : grid_aligned_group(gsz, a.nkb, a.units < sms ? a.units : sms);
         a.timeout_ns = wait_timeout_ns();
+        a.withhold = WITHHOLD_NONE;
+#if FA_TEST_WITHHOLD
+        a.withhold = test_withhold_take(WITHHOLD_BWD_DKV, WITHHOLD_BWD_DKV);
+#endif
         a.det_bound = det ? ws.bound : nullptr;
         a.left = mask.left;
         a.right = mask.right;

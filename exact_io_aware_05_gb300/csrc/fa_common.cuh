@@ -133,15 +133,32 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
         return mbar_wait_slow(bar, parity, ctx, site);
 }
 
+// The same wait for roles whose warps run warp-collective instructions (tensor-memory
+// loads, shuffles, votes) after it: the lanes vote, so the whole warp goes on only when
+// every lane saw the phase complete, and leaves together otherwise.  Lanes of one warp
+// can see different outcomes when a wait gives up: one lane may see the phase complete
+// while another, polling a moment earlier, has seen the abort flag.  Every lane of the
+// warp must call it.
+template <bool kInline = false>
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const WaitCtx &ctx, int site)
+{
+    return __all_sync(0xffffffffu, mbar_wait<kInline>(bar, parity, ctx, site));
+}
+
+// Limit of the teardown waits below, fixed and independent of the main waits' limit
+// (which a caller may shorten): copies and MMAs already issued complete in
+// microseconds, whatever the other roles of the CTA do.
+constexpr uint64_t kDrainTimeoutNs = 4000000000ull;
+
 // Teardown variant: bounded by time only (ignores the abort flag), used to
 // drain copies and MMAs still in flight before the CTA releases its memory.
-static __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns)
+static __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity)
 {
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity))
             return true;
-        if ((it & 31u) == 0u && globaltimer_ns() - t0 > timeout_ns)
+        if ((it & 31u) == 0u && globaltimer_ns() - t0 > kDrainTimeoutNs)
             return false;
     }
 }

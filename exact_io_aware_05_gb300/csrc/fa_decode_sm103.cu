@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(32) decode_kernel(const __grid_constant__ CUte
     int k = 0;
     bool ok = true;
     for (; k < nt; ++k) {
-        if (!mbar_wait(bar0 + 8u * (uint32_t)(k % C::DNS), (uint32_t)(k / C::DNS) & 1u, ctx, SITE_DEC_FULL)) {
+        if (!mbar_wait_warp(bar0 + 8u * (uint32_t)(k % C::DNS), (uint32_t)(k / C::DNS) & 1u, ctx, SITE_DEC_FULL)) {
             ok = false;
             break;
         }
@@ -248,7 +248,7 @@ __global__ void __launch_bounds__(32) decode_kernel(const __grid_constant__ CUte
         // copies already issued land before the CTA exits
         if (lane == 0)
             for (int kk = k; kk < nt && kk < k + C::DNS; ++kk)
-                mbar_wait_drain(bar0 + 8u * (uint32_t)(kk % C::DNS), (uint32_t)(kk / C::DNS) & 1u, a.timeout_ns);
+                mbar_wait_drain(bar0 + 8u * (uint32_t)(kk % C::DNS), (uint32_t)(kk / C::DNS) & 1u);
         return;
     }
 #pragma unroll

@@ -145,6 +145,7 @@ struct FwdArgs {
     int units;           // BH * nqb
     int group;           // heads per L2 group
     uint64_t timeout_ns;
+    int withhold;        // test-only build: the arrive this launch leaves out (else 0, unused)
 };
 
 // One unit = NQ consecutive 128-row query tiles of one (b, h).  Tile t visits the KV
@@ -493,9 +494,9 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                 // drain: every copy still in flight lands before the CTA exits
                 const uint32_t lo = n_loads > (uint32_t)NSLOT ? n_loads - NSLOT : 0;
                 for (uint32_t i = lo; i < n_loads; ++i)
-                    mbar_wait_drain(bar(L::B_FULL + i % NSLOT), (i / NSLOT) & 1, a.timeout_ns);
+                    mbar_wait_drain(bar(L::B_FULL + i % NSLOT), (i / NSLOT) & 1);
                 if (n_q > 0)
-                    mbar_wait_drain(bar(L::B_QFULL), (n_q - 1) & 1, a.timeout_ns);
+                    mbar_wait_drain(bar(L::B_QFULL), (n_q - 1) & 1);
             }
             __syncwarp();
         } else if (NQ == 2 && (warp == 1 || warp == 2)) {
@@ -560,7 +561,13 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                                     mma_ss(tmem + s_col, qd + off, kd + offk, L::IDESC_S, kk > 0 ? 1u : 0u);
                             }
                             tc_commit(bar(L::B_SFULL + t));
-                            tc_commit(bar(L::B_EMPTY + ks));
+#if FA_TEST_WITHHOLD
+                            const bool hold = a.withhold == WITHHOLD_FWD_KV && blockIdx.x == 0 && t == 0 && sn == 0;
+#else
+                            constexpr bool hold = false;
+#endif
+                            if (!hold)
+                                tc_commit(bar(L::B_EMPTY + ks));
                             if (j == me.last)
                                 tc_commit(bar(L::B_QEMPTY));
                             ++sn;
@@ -602,14 +609,20 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                             tc_commit(bar(L::B_EMPTY + vs));
                             ++pvn;
                             if (j == me.last) {
-                                tc_commit(bar(L::B_OFINAL + t));
+#if FA_TEST_WITHHOLD
+                                const bool hold = a.withhold == WITHHOLD_FWD_EPI && blockIdx.x == 0 && t == 0 && epi == 0;
+#else
+                                constexpr bool hold = false;
+#endif
+                                if (!hold)
+                                    tc_commit(bar(L::B_OFINAL + t));
                                 ++epi;
                             }
                             return true;
                         });
                 }
                 tc_commit(drain_bar);
-                mbar_wait_drain(drain_bar, 0, a.timeout_ns);
+                mbar_wait_drain(drain_bar, 0);
             }
             __syncwarp();
         } else if (NQ == 1 && warp == 1) {
@@ -702,7 +715,7 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                 }
                 // drain: all issued MMAs complete before tensor memory is released
                 tc_commit(bar(L::B_DRAIN));
-                mbar_wait_drain(bar(L::B_DRAIN), 0, a.timeout_ns);
+                mbar_wait_drain(bar(L::B_DRAIN), 0);
             }
             __syncwarp();
         }
@@ -748,7 +761,7 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                 // S buffers alternate between consecutive jobs
                 const uint32_t b = NQ == 2 ? (uint32_t)t : (pv & 1);
                 const uint32_t ph = NQ == 2 ? (pv & 1) : ((pv >> 1) & 1);
-                if (!mbar_wait<INL>(bar(L::B_SFULL + b), ph, ctx, SITE_S_SFULL)) {
+                if (!mbar_wait_warp<INL>(bar(L::B_SFULL + b), ph, ctx, SITE_S_SFULL)) {
                     ok = false;
                     break;
                 }
@@ -842,7 +855,7 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                 // them).  One tile: P goes over the first columns of this S buffer.
                 uint8_t *prow = smem + L::OFF_P + t * L::P_TILE + rit * 128;
                 if constexpr (F8) {   // measured faster with the wait ahead of the exponentials
-                    if (pv > 0 && !mbar_wait<INL>(bar(L::B_ODONE + t), (pv - 1) & 1, ctx, SITE_S_ODONE)) {
+                    if (pv > 0 && !mbar_wait_warp<INL>(bar(L::B_ODONE + t), (pv - 1) & 1, ctx, SITE_S_ODONE)) {
                         ok = false;
                         break;
                     }
@@ -879,7 +892,7 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                         tmem_st_x16(lane_base + L::S_COL + b * BC + c * 16, pk);
                 }
                 if constexpr (L::PSM) {
-                    if (!F8 && pv > 0 && !mbar_wait<INL>(bar(L::B_ODONE + t), (pv - 1) & 1, ctx, SITE_S_ODONE)) {
+                    if (!F8 && pv > 0 && !mbar_wait_warp<INL>(bar(L::B_ODONE + t), (pv - 1) & 1, ctx, SITE_S_ODONE)) {
                         ok = false;
                         break;
                     }
@@ -904,7 +917,7 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                 if (__any_sync(0xffffffffu, resc)) {
                     // O~ must hold the previous PV of this tile before it is rescaled (two tiles:
                     // waited for above)
-                    if (!L::PSM && !mbar_wait<INL>(bar(L::B_ODONE + t), (pv - 1) & 1, ctx, SITE_S_ODONE)) {
+                    if (!L::PSM && !mbar_wait_warp<INL>(bar(L::B_ODONE + t), (pv - 1) & 1, ctx, SITE_S_ODONE)) {
                         ok = false;
                         break;
                     }
@@ -945,7 +958,7 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
             // epilogue: O = O~ / l, lse = c m + ln l.  With one tile the softmax can be up
             // to two PVs ahead of the tensor core here, too far for a parity wait on the
             // per-PV barrier; the per-unit barrier completes exactly once per epilogue.
-            if (!mbar_wait<INL>(bar(L::B_OFINAL + t), ep & 1, ctx, SITE_S_EPI))
+            if (!mbar_wait_warp<INL>(bar(L::B_OFINAL + t), ep & 1, ctx, SITE_S_EPI))
                 break;
             ++ep;
             tc_fence_after();
@@ -1034,6 +1047,11 @@ int launch(const void *q, const void *k, const void *v, void *o, float *lse, int
     g = g < 1 ? 1 : (g > BH ? BH : g);
     a.group = a.masked ? g : grid_aligned_group(g, a.nqb, grid);
     a.timeout_ns = wait_timeout_ns();
+    a.withhold = WITHHOLD_NONE;
+#if FA_TEST_WITHHOLD
+    if (L::NQ == 2)
+        a.withhold = test_withhold_take(WITHHOLD_FWD_KV, WITHHOLD_FWD_EPI);
+#endif
     auto kernel = a.masked ? fwd_kernel<D, true> : fwd_kernel<D, false>;
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES) != cudaSuccess)
         return ERR_CUDA;
@@ -1084,6 +1102,7 @@ int launch_f8(const void *q8, const void *k8, const void *vt8, const float *qd, 
     const int grid = a.units < device_sm_count() ? a.units : device_sm_count();
     a.group = grid_aligned_group(g < 1 ? 1 : (g > BH ? BH : g), a.nqb, grid);
     a.timeout_ns = wait_timeout_ns();
+    a.withhold = WITHHOLD_NONE;
     auto kernel = fwd_kernel<D, false, true>;
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES) != cudaSuccess)
         return ERR_CUDA;

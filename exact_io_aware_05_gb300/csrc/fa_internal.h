@@ -21,6 +21,26 @@ int encode_tmap_3d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype
 
 int device_sm_count();          // SMs of the current device (cached per device)
 uint64_t wait_timeout_ns();     // bounded-wait limit for device spin waits
+
+// Test-only build of the library (compiled with FA_TEST_WITHHOLD=1 into a separate
+// shared object; the product library is built without it and has none of this): one
+// launch may leave out one mbarrier arrive, so that a bounded wait of one CTA runs out
+// and the timeout path (abort flag, drains, status word) runs.  The case is armed from
+// the host, once, and taken by the next launch of the matching kernel:
+//   WITHHOLD_FWD_KV   forward, CTA 0: query tile 0's release of its first K/V slot;
+//                     the producer waits for that slot again (the MMA issuers and the
+//                     softmax then wait for copies that never come)
+//   WITHHOLD_FWD_EPI  forward, CTA 0: the "O~ final" signal of query tile 0 in the first
+//                     unit; only that tile's softmax waits for it (epilogue)
+//   WITHHOLD_BWD_DKV  backward tile loop, CTA 0: the "dK, dV complete" signal of its
+//                     first unit; only the drain warpgroup waits for it
+#ifndef FA_TEST_WITHHOLD
+#define FA_TEST_WITHHOLD 0
+#endif
+enum : int { WITHHOLD_NONE = 0, WITHHOLD_FWD_KV = 1, WITHHOLD_FWD_EPI = 2, WITHHOLD_BWD_DKV = 3 };
+#if FA_TEST_WITHHOLD
+int test_withhold_take(int lo, int hi);   // the armed case if in [lo, hi] (then disarmed), else 0
+#endif
 // Heads per group of a persistent kernel's unit order.  gmax keeps the group's
 // tensors within the L2 budget; where a group size in [gmax/2, gmax] makes a group
 // a whole number of passes over the grid (levels units per head), the snake order
@@ -78,12 +98,16 @@ struct BwdWorkspace {
     int *bound;      // [BH][Tq_pad / 128]
 };
 size_t bwd_row_stride(int Tq);
-size_t bwd_workspace_bytes(int BH, int Tq, int d);
+size_t bwd_workspace_bytes(size_t BH, int Tq, int d);
 BwdWorkspace bwd_workspace_carve(void *ws, int BH, int Tq, int d);
 // stages: bit 0 = preprocess (D, lse2, zero dQ accumulator; fixed-point bounds),
 // bit 1 = tile loop (dK, dV, dQ accumulation), bit 2 = dQ scale-and-round;
 // kBwdDeterministic: dQ is accumulated as int32 fixed point (order-independent sums).
 constexpr int kBwdDeterministic = 8;
+// Every check of fa_bwd's arguments except the workspace's and the device's (no CUDA call).
+int bwd_check_args(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dO,
+                   const void *dq, const void *dk, const void *dv, int B, int H, int Tq, int Tk, int d,
+                   const MaskSpec &mask, float scale);
 int bwd_launch(const void *q, const void *k, const void *v, const void *o, const float *lse,
                const void *dO, void *dq, void *dk, void *dv, int BH, int Tq, int Tk, int d,
                const MaskSpec &mask, float scale, const BwdWorkspace &ws, int stages, cudaStream_t s);

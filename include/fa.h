@@ -233,8 +233,10 @@ int fa_bwd_stage(int stage, const void *q, const void *k, const void *v, const v
 
 /*
  * Size of the fixed device scratch array behind fa_bwd_noalloc (64 MiB).  It
- * holds fa_bwd_workspace_bytes(B, H, Tq, Tk, d) bytes when, for example,
- * B*H*Tq_pad <= 126,000 rows at d = 128 (B8 H8 T2048, B1 H32 T3840).
+ * holds fa_bwd_workspace_bytes(B, H, Tq, Tk, d) bytes, about 520 bytes per
+ * padded query row at d = 128 and 264 at d = 64, when B*H*Tq_pad is at most
+ * about 129,000 rows at d = 128 (B8 H8 T1920, B1 H32 T3840; not B8 H8 T2048)
+ * or 254,000 rows at d = 64 (B8 H16 T1920), where Tq_pad rounds Tq up to 128.
  */
 #define FA_BWD_NOALLOC_SCRATCH_BYTES (64u << 20)
 
@@ -248,12 +250,17 @@ int fa_bwd_stage(int stage, const void *q, const void *k, const void *v, const v
  * the scratch comes from a fixed array of FA_BWD_NOALLOC_SCRATCH_BYTES that
  * the library keeps in device memory (each device holds it until the process
  * exits).  The call allocates nothing.
- *   - Sizes whose fa_bwd_workspace_bytes(...) exceeds
- *     FA_BWD_NOALLOC_SCRATCH_BYTES return FA_ERR_UNSUPPORTED before any CUDA
- *     call; use fa_bwd with a caller-owned workspace for those.
+ *   - Arguments are checked as fa_bwd checks them (FA_ERR_INVALID_ARG,
+ *     FA_ERR_UNSUPPORTED for d = 256) before anything else.  Then sizes whose
+ *     fa_bwd_workspace_bytes(...) exceeds FA_BWD_NOALLOC_SCRATCH_BYTES return
+ *     FA_ERR_UNSUPPORTED, still before any CUDA call; use fa_bwd with a
+ *     caller-owned workspace for those.
  *   - The first call on a device looks the array's device address up
- *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before any stream capture.
+ *     (cudaGetSymbolAddress, with that device current) and caches it with the
+ *     current CUDA context; make that first call before any stream capture.
+ *     A call under a different context (after cudaDeviceReset, for one) looks
+ *     the address up again, so make the first call after a reset before any
+ *     capture too.
  *   - Every call on a device shares the one array.  Each call rewrites all of
  *     the scratch it uses before reading it (the dQ accumulator is zeroed),
  *     so nothing carries over between calls, but calls that overlap on the

@@ -92,3 +92,17 @@ def check_grads(w, x, grads, heads, rows=None, keys=None, tol=TOL_GRAD):
     for n in worst:
         assert worst[n] <= tol, (n, worst, raw)
     return raw, worst
+
+
+def assert_same_up_to_add_order(got: torch.Tensor, want: torch.Tensor, what: str = "dq") -> None:
+    """Two bf16 results of the same fp32 sums added in different orders (the dQ reduce-adds
+    land in whatever order the thread blocks reach them): each element within one bf16 ulp of
+    the larger magnitude, plus 1e-5 of the tensor's largest magnitude for fp32 partial sums
+    that cancel near zero."""
+    a = got.detach().float().cpu().double().numpy()
+    b = want.detach().float().cpu().double().numpy()
+    m = np.maximum(np.abs(a), np.abs(b))
+    ulp = np.where(m > 0, np.exp2(np.floor(np.log2(np.where(m > 0, m, 1.0))) - 7), 0.0)
+    floor = 1e-5 * float(np.abs(b).max()) if b.size else 0.0
+    bad = np.abs(a - b) > ulp + floor
+    assert not bad.any(), (what, int(bad.sum()), float(np.abs(a - b).max()))

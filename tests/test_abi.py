@@ -142,3 +142,57 @@ def test_fp8_host_validation(lib):
     overlap = [outs[0], outs[0]] + outs[2:]
     assert lib.fa_fp8_quantize(*q, None, 1, 1, 64, 64, 128, *overlap, None) == 1
     assert lib.fa_fp8_quantize(*q, None, 1, 1, 0, 0, 128, *outs, None) == 0
+
+
+def _noalloc(lib):
+    f = lib.fa_bwd_noalloc
+    vp, i = ctypes.c_void_p, ctypes.c_int
+    f.argtypes = [vp] * 9 + [i] * 6 + [ctypes.c_float, vp]
+    f.restype = i
+    return f
+
+
+def _far_apart(n, base=1 << 40, step=1 << 34):
+    """Fake, aligned, non-overlapping device addresses, never dereferenced on these paths."""
+    return [base + step * i for i in range(n)]
+
+
+def test_noalloc_scratch_examples_in_header(lib):
+    """The sizes include/fa.h names as fitting the 64 MiB scratch do fit; the one it names
+    as not fitting does not."""
+    lib.fa_bwd_workspace_bytes.argtypes = [ctypes.c_int] * 5
+    lib.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
+    text = open(HEADER).read()
+    limit = int(re.search(r"#define FA_BWD_NOALLOC_SCRATCH_BYTES \((\d+)u << (\d+)\)", text).expand(r"\1")) << 20
+    assert limit == 64 << 20
+    for B, H, T, d in ((8, 8, 1920, 128), (1, 32, 3840, 128), (8, 16, 1920, 64)):
+        assert f"B{B} H{H} T{T}" in text
+        assert lib.fa_bwd_workspace_bytes(B, H, T, T, d) <= limit, (B, H, T, d)
+    assert "not B8 H8 T2048" in text
+    assert lib.fa_bwd_workspace_bytes(8, 8, 2048, 2048, 128) > limit
+    # the row figures the header quotes: per-row bytes and the largest row counts
+    per_row = {128: 520, 64: 264}
+    for d, rows in ((128, 129_000), (64, 254_000)):
+        assert abs(limit / per_row[d] - rows) < 0.01 * rows
+
+
+def test_noalloc_checks_arguments_before_its_scratch_limit(lib):
+    """fa_bwd_noalloc reports fa_bwd's argument errors even for sizes beyond its scratch,
+    and only then FA_ERR_UNSUPPORTED for the size; none of this makes a CUDA call."""
+    f = _noalloc(lib)
+    ptrs = _far_apart(9)
+    big = (8, 32, 4096, 4096, 128)
+    assert f(*ptrs, *big, 1, 0.088, None) == 2                      # beyond the scratch
+    assert f(*ptrs, *big, 1, float("nan"), None) == 1               # bad scale
+    assert f(*ptrs, *big, 2, 0.088, None) == 1                      # bad causal flag
+    assert f(None, *ptrs[1:], *big, 1, 0.088, None) == 1            # null q
+    assert f(ptrs[0] + 2, *ptrs[1:], *big, 1, 0.088, None) == 1     # misaligned q
+    assert f(*ptrs[:6], ptrs[0], *ptrs[7:], *big, 1, 0.088, None) == 1   # dq overlaps q
+    assert f(*ptrs, 8, 32, 4096, 4096, 256, 1, 0.088, None) == 2    # d = 256 backward
+
+
+def test_bwd_workspace_bytes_rejects_head_overflow(lib):
+    lib.fa_bwd_workspace_bytes.argtypes = [ctypes.c_int] * 5
+    lib.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
+    assert lib.fa_bwd_workspace_bytes(1 << 16, 1 << 16, 1, 1, 64) == 0   # B*H beyond 32 bits
+    assert lib.fa_bwd_workspace_bytes(1 << 15, 1 << 15, 1, 1, 64) > 0

@@ -121,3 +121,22 @@ def test_bwd_long_context(fa, name):
     rows = rows_of(w.Tq, 48)
     keys = rows_of(w.Tk, 48, seed=1)
     check_grads(w, x, (dq, dk, dv), [(0, 0)], rows=rows, keys=keys)
+
+
+@pytest.mark.parametrize("B,H,T,d,causal", [(2, 4, 1000, 128, True), (1, 3, 777, 64, False)])
+def test_stages_equal_fa_bwd(fa, B, H, T, d, causal):
+    """fa_bwd_stage(1), (2), (3) in order -- the three kernels as bench.py times them -- give
+    fa_bwd's dk and dv bit for bit and its dq up to the order of the fp32 reduce-adds."""
+    from gpu_util import assert_same_up_to_add_order
+    w = inputs.small(B, H, T, T, d, causal, seed=17 + d, backward=True)
+    x = inputs.generate(w, device="cuda")
+    q, k, v, do = x["q"], x["k"], x["v"], x["do"]
+    o, lse = fa.attention_forward(q, k, v, causal, w.scale)
+    ref = fa.attention_backward(q, k, v, o, lse, do, causal, w.scale)
+    ws = fa.alloc_workspace(B, H, T, T, d, q.device)
+    dq, dk, dv = (torch.full_like(t, float("nan")) for t in (q, k, v))
+    for stage in (1, 2, 3):
+        fa.fa_bwd_stage(stage, q, k, v, o, lse, do, dq, dk, dv, causal, w.scale, ws)
+    assert fa.fa_sync_status() == fa.FA_OK
+    assert torch.equal(dk, ref[1]) and torch.equal(dv, ref[2])
+    assert_same_up_to_add_order(dq, ref[0])

@@ -107,3 +107,68 @@ def test_memory_arithmetic():
     assert b["B"] * b["H"] * b["T"] ** 2 * b["bytes_per_value"] == b["printed_gb"] * 2**30
     w = g["wide_tile"]
     assert w["rows"] * w["d"] * w["bytes_per_value"] == w["printed_bytes"]
+
+
+def test_fa1_order_count_by_hand():
+    """The FA1-order count (key blocks outside) against loads and stores enumerated by hand
+    on a 4 x 4 grid of tiles: zerotofrontier "FlashAttention", "The IO complexity theorem"
+    (each K_j, V_j loaded once; per key block, each query block loads Q_i, O_i, l_i, m_i and
+    writes O_i, l_i, m_i back).  T = 8, d = 2, B_c = 2 (n_c = 4), query blocks of 2 rows:
+      K_j, V_j loads: 4 key blocks x (2 x 2 + 2 x 2)                 =  32
+      per (i, j): loads Q_i 4 + O_i 4 + l_i 2 + m_i 2 = 12,
+                  stores O_i 4 + l_i 2 + m_i 2 = 8;   16 tiles x 20  = 320
+    total 352.  Ragged: T = 5, d = 3, B_c = 2 (n_c = 3): K, V 2 x 5 x 3 = 30; each sweep
+    loads Q 15 + O 15 + l 5 + m 5 and stores O 15 + l 5 + m 5 = 65; 3 sweeps = 195; total 225."""
+    assert tiled.fa1_order_accesses(8, 2, 2) == 32 + 16 * (12 + 8) == 352
+    assert tiled.fa1_order_accesses(5, 3, 2) == 30 + 3 * 65 == 225
+    # one block holds every key: a single sweep, K and V loaded once
+    assert tiled.fa1_order_accesses(8, 2, 8) == 32 + (3 * 16 + 4 * 8) == 112
+
+
+# Backward traffic enumerated by hand (zerotofrontier "FlashAttention", "The backward pass,
+# derived": D in one pass over dO and O; key blocks outside, each K_j, V_j loaded once, dK_j,
+# dV_j written once; per visited tile Q_i, dO_i, lse_i, D_i loaded and dQ_i read, added to
+# and written back).  Each case: (Tq, Tk, d, Br, Bc, causal, reads, writes, tiles visited).
+BWD_HAND = [
+    # T = 8, d = 2, 4 x 4 blocks, 2 x 2 tiles.  reads: dO 16 + O 16; per key block K 8 + V 8;
+    # per tile Q 8 + dO 8 + lse 4 + D 4 + dQ 8 = 32.  writes: D 8; per tile dQ 8; per key
+    # block dK 8 + dV 8.  Non-causal, 4 tiles: reads 32 + 2 x 16 + 4 x 32 = 192,
+    # writes 8 + 4 x 8 + 2 x 16 = 72.
+    (8, 8, 2, 4, 4, False, 192, 72, 4),
+    # causal: tile (query block 0, key block 1) is skipped (first key 4 > last row 3), 3 tiles:
+    # reads 32 + 32 + 3 x 32 = 160, writes 8 + 3 x 8 + 32 = 64
+    (8, 8, 2, 4, 4, True, 160, 64, 3),
+    # Tq = 6, Tk = 10, bottom-right causal (offset 4), d = 2, 4 x 4 blocks with ragged tails.
+    # Query block 0 (rows 0-3, last allowed key 7) skips key block 2 (keys 8-9); query block 1
+    # (rows 4-5) sees all three.  reads: dO 12 + O 12; K, V 16 + 16 + 8; tiles of 4 rows
+    # 4 x (2 + 2 + 1 + 1 + 2) = 32 (two of them), of 2 rows 16 (three): 24 + 40 + 64 + 48 = 176.
+    # writes: D 6; dQ 8 + 8 + 4 + 4 + 4 = 28; dK, dV 16 + 16 + 8 = 40: 74.
+    (6, 10, 2, 4, 4, True, 176, 74, 5),
+]
+
+
+@pytest.mark.parametrize("Tq,Tk,d,Br,Bc,causal,reads,writes,tiles", BWD_HAND)
+def test_backward_counter_by_hand(Tq, Tk, d, Br, Bc, causal, reads, writes, tiles):
+    q, k, v, dO = _inputs(Tq, Tk, d, seed=3, dO=True)
+    g = oracle.attention_bwd(q, k, v, dO, causal, 0.5, want_o=True)
+    *_, cnt = tiled.flash_backward(q, k, v, g["o"], dO, g["lse"], Br, Bc, causal, 0.5)
+    assert (cnt.reads, cnt.writes) == (reads, writes)
+    assert tiles == sum(1 for i in range(math.ceil(Tq / Br)) for j in range(math.ceil(Tk / Bc))
+                        if not (causal and j * Bc > min((i + 1) * Br, Tq) - 1 + Tk - Tq))
+
+
+def test_backward_traffic_has_no_square_term():
+    """zerotofrontier "The backward pass, derived": the backward's traffic is a few dozen
+    times T d, with no T^2 term.  At fixed block sizes the count per T d grows with the
+    number of key blocks only (T / B_c), never with T^2 / d."""
+    d, Br, Bc = 64, 128, 64
+    per_td = []
+    for T in (512, 1024):
+        q, k, v, dO = _inputs(T, T, d, seed=T, dO=True)
+        g = oracle.attention_bwd(q, k, v, dO, False, 0.125, want_o=True)
+        *_, cnt = tiled.flash_backward(q, k, v, g["o"], dO, g["lse"], Br, Bc, False, 0.125)
+        per_td.append(cnt.total / (T * d))
+        # exact: D pass 2Td + T; K, V 2Td; n_c sweeps of (4Td + 2T); dK, dV 2Td
+        n_c = T // Bc
+        assert cnt.total == 2 * T * d + T + 2 * T * d + n_c * (4 * T * d + 2 * T) + 2 * T * d
+    assert 12 < per_td[0] < per_td[1] < 100   # "a few dozen times T d"

@@ -2,17 +2,21 @@
 memory (a plug-in whose host framework owns all device memory, or latency-
 critical code that cannot take cudaMalloc's implicit synchronisation).  It
 takes its scratch from a fixed array inside the library instead of a caller
-workspace.  Called here through the C ABI (ctypes) and compared with fa_bwd,
-twice in a row, because every call shares that array and must not depend on
-what the previous call left in it.  This file is collected last so that a run
-stopping at the first failure has already run every other test."""
+workspace.  Called here through the C ABI (ctypes) and compared with fa_bwd on
+the same inputs, twice in a row, because every call shares that array and must
+not depend on what the previous call left in it.  Both run the same kernels, so
+dk and dv must be bitwise equal and dq may differ only by the order in which
+its fp32 reduce-adds landed.  The host-side checks (argument errors before the
+scratch limit, sizes beyond it) need no GPU and live in test_abi.py.  This file
+is collected last so that a run stopping at the first failure has already run
+every other test."""
 import ctypes
 
 import pytest
 import torch
 
 from exact_io_aware_05_gb300 import inputs
-from gpu_util import TOL_GRAD
+from gpu_util import assert_same_up_to_add_order
 
 pytestmark = pytest.mark.gpu
 
@@ -42,18 +46,6 @@ def test_noalloc_matches_fa_bwd_twice(B, H, T, d, causal):
                dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, T, T, d, int(causal), w.scale, stream)
         assert st == 0, fa.fa_status_string(st)
         assert fa.fa_sync_status() == fa.FA_OK
-        for name, got, want in (("dq", dq, ref[0]), ("dk", dk, ref[1]), ("dv", dv, ref[2])):
-            err = (got.float() - want.float()).abs().max().item()
-            assert err <= TOL_GRAD, (call, name, err)
-
-
-def test_noalloc_rejects_sizes_beyond_its_scratch():
-    from exact_io_aware_05_gb300 import fa
-    lib = ctypes.CDLL(fa.LIB_PATH)
-    f = _noalloc(lib)
-    limit = 64 << 20
-    B, H, T, d = 8, 32, 4096, 128
-    assert fa.fa_bwd_workspace_bytes(B, H, T, T, d) > limit
-    p = 1 << 20   # never dereferenced: the size check comes first
-    st = f(*[p + 4096 * n for n in range(9)], B, H, T, T, d, 1, 0.088, None)
-    assert st == fa.FA_ERR_UNSUPPORTED
+        assert torch.equal(dk, ref[1]), ("dk", call)
+        assert torch.equal(dv, ref[2]), ("dv", call)
+        assert_same_up_to_add_order(dq, ref[0], f"dq call {call}")
