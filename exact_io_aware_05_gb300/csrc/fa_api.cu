@@ -45,23 +45,42 @@ int encode_tmap_3d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype
                                   box_inner, box_rows);
 }
 
-int encode_tmap_3d_strided(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes,
-                           uint64_t inner, uint64_t rows, uint64_t planes, uint64_t row_stride, uint32_t box_inner,
-                           uint32_t box_rows)
+namespace {
+
+int encode_3d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, uint64_t inner, uint64_t rows,
+              uint64_t planes, uint64_t row_stride, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swz)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn)
         return ERR_CUDA;
-    (void)elem_bytes;
     const cuuint64_t dims[3] = {inner, rows, planes};
     const cuuint64_t strides[2] = {row_stride, rows * row_stride};
     const cuuint32_t box[3] = {box_inner, box_rows, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     const CUresult r = fn(map, dtype, 3, const_cast<void *>(base), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? OK : ERR_CUDA;
 }
+
+}  // namespace
+
+int encode_tmap_3d_plain(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes,
+                         uint64_t inner, uint64_t rows, uint64_t planes, uint32_t box_inner, uint32_t box_rows)
+{
+    return encode_3d(map, base, dtype, inner, rows, planes, inner * (uint64_t)elem_bytes, box_inner, box_rows,
+                     CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+int encode_tmap_3d_strided(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes,
+                           uint64_t inner, uint64_t rows, uint64_t planes, uint64_t row_stride, uint32_t box_inner,
+                           uint32_t box_rows)
+{
+    (void)elem_bytes;
+    return encode_3d(map, base, dtype, inner, rows, planes, row_stride, box_inner, box_rows,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 
 int device_sm_count()
 {

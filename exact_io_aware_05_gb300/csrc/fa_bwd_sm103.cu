@@ -213,20 +213,6 @@ __device__ __forceinline__ void fence_proxy_async_smem()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Named barrier 1 over the 128 threads of the drain warpgroup: plain, and with the AND of
-// a predicate (every thread gets the same answer, so all take the same branch after it).
-__device__ __forceinline__ void drain_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-__device__ __forceinline__ bool drain_all(bool v)
-{
-    uint32_t r;
-    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
-                 "bar.red.and.pred p, 1, 128, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-                 : "=r"(r)
-                 : "r"((uint32_t)v)
-                 : "memory");
-    return r != 0;
-}
-
 // Bulk reduce-add of `bytes` from shared memory into global memory by the TMA engine
 // (fp32 add, or 32-bit integer add for the fixed-point accumulator), in a bulk group.
 __device__ __forceinline__ void bulk_reduce_add_f32(void *dst, uint32_t src, uint32_t bytes)
@@ -293,7 +279,8 @@ template <int D, bool MASKED>
 __global__ void __launch_bounds__(512, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                    const BwdArgs a)
+                    const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
+                    const __grid_constant__ CUtensorMap tm_acc, const BwdArgs a)
 {
     using L = BwdLayout<D>;
     constexpr int NST = L::NST;
@@ -336,6 +323,9 @@ __global__ void __launch_bounds__(512, 1)
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
         tma_prefetch_desc(&tm_do);
+        tma_prefetch_desc(&tm_dk);
+        tma_prefetch_desc(&tm_dv);
+        tma_prefetch_desc(&tm_acc);
     }
     if (warp == 0) {
         tmem_alloc(smem_u32(tmem_slot), L::TMEM_COLS);
@@ -694,8 +684,7 @@ __global__ void __launch_bounds__(512, 1)
         const int row = (int)(quarter * 32 + lane);      // TMEM lane
         const uint32_t lane_base = tmem + ((quarter * 32u) << 16);
         uint32_t g = 0, nu = 0;
-        uint32_t stg_n = 0;                          // dQ chunks staged so far (BULK)
-        const bool lead = warp == 12 && lane == 0;   // issues the bulk reduce-adds
+        uint32_t stg_n = 0;                          // dQ boxes this warp has staged (d = 128)
         bool ok = true;
         for (int pass = 0, u = snake_unit<!MASKED>(0); u < a.units && ok; u = snake_unit<!MASKED>(++pass)) {
             const Unit x = make_unit<MASKED>(u, a);
@@ -715,11 +704,8 @@ __global__ void __launch_bounds__(512, 1)
             for (int i = 0, qi = x.i0; i < x.nq; ++i, ++g, qi = MASKED ? unit_next(x, qi + 1, a.nkbm) : qi + 1) {
                 const uint32_t b = L::DQ_ALIAS ? 0u : (g & 1u);
                 const uint32_t ph = L::DQ_ALIAS ? (g & 1u) : ((g >> 1) & 1u);
-                bool got = mbar_wait<true>(bar(L::B_DQFULL + b), ph, ctx, SITE_D_DQFULL);
-                if constexpr (L::BULK)
-                    got = drain_all(got);   // one decision for the warpgroup (named barriers follow)
-                else
-                    got = __all_sync(0xffffffffu, got);   // one decision for the warp (tensor-memory loads follow)
+                // one decision for the warp (tensor-memory loads follow)
+                const bool got = __all_sync(0xffffffffu, mbar_wait<true>(bar(L::B_DQFULL + b), ph, ctx, SITE_D_DQFULL));
                 if (!got) {
                     ok = false;
                     break;
@@ -746,32 +732,30 @@ __global__ void __launch_bounds__(512, 1)
                     tmem_wait_ld_x32(vd);
                     tc_fence_before();
                     mbar_arrive(bar(L::B_DQEMPTY));
-                    // Named barrier 1 (the drain warpgroup's 128 threads, all on the same path)
-                    // orders each chunk: its buffer's previous reduce-add has read it, then every
-                    // thread has written its part.
+                    // Each warp stages its 32 features of a chunk of 32 queries as a 4 KB box
+                    // ([query][feature], 128-byte rows: a warp writes one row per instruction) in its
+                    // own two buffers and its lane 0 hands the box to the TMA engine as a tensor
+                    // reduce-add; the four warps never wait for one another.
                     auto stage_chunk = [&](const uint32_t(&v)[32], int c) {
                         const uint32_t sb = stg_n & 1u;
-                        if (lead && stg_n >= 2)
-                            bulk_wait_read_1();   // the chunk two back, in this buffer, has been read
-                        drain_sync();
-                        uint32_t *dst = reinterpret_cast<uint32_t *>(smem + L::OFF_STG + sb * L::STG_BYTES) + row;
+                        const uint32_t boff = L::OFF_STG + quarter * 8192u + sb * 4096u;
+                        if (lane == 0 && stg_n >= 2)
+                            bulk_wait_read_1();   // the box two back, in this buffer, has been read
+                        __syncwarp();
+                        uint32_t *dst = reinterpret_cast<uint32_t *>(smem + boff) + lane;
                         if (a.det_bound) {
 #pragma unroll
                             for (int e = 0; e < 32; ++e)
-                                dst[e * D] = (uint32_t)__float2int_rn(__uint_as_float(v[e]) * dsc);
+                                dst[e * 32] = (uint32_t)__float2int_rn(__uint_as_float(v[e]) * dsc);
                         } else {
 #pragma unroll
                             for (int e = 0; e < 32; ++e)
-                                dst[e * D] = v[e];
+                                dst[e * 32] = v[e];
                         }
                         fence_proxy_async_smem();
-                        drain_sync();
-                        if (lead) {
-                            const uint32_t src = sbase + L::OFF_STG + sb * L::STG_BYTES;
-                            if (a.det_bound)
-                                bulk_reduce_add_u32(iacc + (size_t)c * 32 * D, src, L::STG_BYTES);
-                            else
-                                bulk_reduce_add_f32(acc + (size_t)c * 32 * D, src, L::STG_BYTES);
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_reduce_add_3d(&tm_acc, sbase + boff, (int)quarter * 32, qb + c * 32, x.bh);
                             bulk_commit();
                         }
                         ++stg_n;
@@ -825,44 +809,101 @@ __global__ void __launch_bounds__(512, 1)
             }
             if (!ok)
                 break;
-            bool kv_ok = mbar_wait<true>(bar(L::B_DKVFULL), nu & 1, ctx, SITE_D_DKVFULL);
-            if constexpr (L::BULK)
-                kv_ok = drain_all(kv_ok);
-            else
-                kv_ok = __all_sync(0xffffffffu, kv_ok);
+            const bool kv_ok = __all_sync(0xffffffffu, mbar_wait<true>(bar(L::B_DKVFULL), nu & 1, ctx, SITE_D_DKVFULL));
             if (!kv_ok)
                 break;
             tc_fence_after();
+            // dV, then dK (x c): each warp packs its 32 key rows (the TMEM lanes it reads) to bf16
+            // into its own 8 KB of shared memory (d = 128: a quarter of the two staging buffers,
+            // free once the last dQ chunk has been read; d = 64: the warp's own buffer) as boxes of
+            // 32 rows x 64 columns with the 128-byte swizzle, and its lane 0 hands them to the TMA
+            // engine as tensor stores (rows past Tk are not written).  This keeps the 64 KB per
+            // unit off the load/store path that the softmax of the next unit is using.  Both
+            // accumulators are read out of tensor memory first (at d = 128 dK waits in registers
+            // while dV is stored), so the next unit's dV and dK may overwrite them at once.
+            if (lane == 0)
+                bulk_wait_read_all();   // this warp's dQ chunks have been read
+            __syncwarp();
+            {
+                const uint32_t wbuf = sbase + L::OFF_STG + quarter * 8192u;
+                uint8_t *wrow = smem + L::OFF_STG + quarter * 8192u + lane * 128;
+                // 32 columns (16 bf16 pairs) of this row at column 32c of a 64-column box grid
+                auto put = [&](uint8_t *boxes, const uint32_t *w, int c) {
+                    uint8_t *box = boxes + (c >> 1) * 4096;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t v[32], w[16];
-                tmem_ld_x32(lane_base + L::T_DV + c * 32, v);
+                    for (int e = 0; e < 4; ++e) {
+                        const int unit = (c & 1) * 4 + e;
+                        *reinterpret_cast<uint4 *>(box + ((unit ^ (lane & 7)) << 4)) =
+                            make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+                    }
+                };
+                uint32_t dkp[L::BULK ? D / 2 : 1];   // d = 128: dK of this row, packed
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    w[e] = pack_bf16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
-                if (l < a.Tk) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(a.dv + krow * D + c * 32);
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t v[32], w[16];
+                    tmem_ld_x32(lane_base + L::T_DV + c * 32, v);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+                    for (int e = 0; e < 16; ++e)
+                        w[e] = pack_bf16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+                    put(wrow, w, c);
                 }
-                tmem_ld_x32(lane_base + L::T_DK + c * 32, v);
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    w[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * a.scale, __uint_as_float(v[2 * e + 1]) * a.scale);
-                if (l < a.Tk) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(a.dk + krow * D + c * 32);
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld_x32(lane_base + L::T_DK + c * 32, v);
+                    if constexpr (L::BULK) {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+                        for (int e = 0; e < 16; ++e)
+                            dkp[c * 16 + e] =
+                                pack_bf16x2(__uint_as_float(v[2 * e]) * a.scale, __uint_as_float(v[2 * e + 1]) * a.scale);
+                    } else {   // d = 64: dK's box right after dV's
+                        uint32_t w[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            w[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * a.scale, __uint_as_float(v[2 * e + 1]) * a.scale);
+                        put(wrow + 4096, w, c);
+                    }
                 }
+                tc_fence_before();
+                mbar_arrive(bar(L::B_DKVEMPTY));   // dV and dK are out of tensor memory
+                // a box whose first row is past Tk has nothing to write and is not issued
+                const bool rows_here = x.j * BK + (int)quarter * 32 < a.Tk;
+                const int y0 = x.j * BK + (int)quarter * 32;
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0 && rows_here) {
+                    if constexpr (L::BULK) {
+                        tma_store_3d(&tm_dv, wbuf, 0, y0, x.bh);
+                        tma_store_3d(&tm_dv, wbuf + 4096, 64, y0, x.bh);
+                    } else {
+                        tma_store_3d(&tm_dv, wbuf, 0, y0, x.bh);
+                        tma_store_3d(&tm_dk, wbuf + 4096, 0, y0, x.bh);
+                    }
+                    bulk_commit();
+                }
+                if constexpr (L::BULK) {
+                    if (lane == 0)
+                        bulk_wait_read_all();   // dV has left the buffer
+                    __syncwarp();
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c)
+                        put(wrow, dkp + c * 16, c);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && rows_here) {
+                        tma_store_3d(&tm_dk, wbuf, 0, y0, x.bh);
+                        tma_store_3d(&tm_dk, wbuf + 4096, 64, y0, x.bh);
+                        bulk_commit();
+                    }
+                }
+                if (lane == 0)
+                    bulk_wait_read_all();   // the buffer is free again for the next unit's dQ
+                __syncwarp();
             }
-            tc_fence_before();
-            mbar_arrive(bar(L::B_DKVEMPTY));
             ++nu;
         }
-        if (L::BULK ? lead : lane == 0)
-            bulk_wait_all();   // every reduce-add has landed and read its shared memory
+        if (lane == 0)
+            bulk_wait_all();   // every reduce-add and store of this warp has completed
     }
     // ------------------------------------------------------------ teardown
     tc_fence_before();
@@ -1062,6 +1103,18 @@ int launch_bwd(const void *q, const void *k, const void *v, const void *o, const
             st = encode_tmap_3d(&tq, Tq > 0 ? q : k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, tq_rows, BH, 64, BQ);
         if (st == OK)
             st = encode_tmap_3d(&tdo, Tq > 0 ? dO : k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, tq_rows, BH, 64, BQ);
+        // dQ accumulator ([BH][Tq_pad][D], fp32 or, deterministic, int32): each drain warp adds
+        // boxes of its 32 features x 32 queries (d = 128)
+        CUtensorMap tacc;
+        if (st == OK)
+            st = encode_tmap_3d_plain(&tacc, ws.dq_acc, det ? CU_TENSOR_MAP_DATA_TYPE_INT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                                      4, D, (uint64_t)(Tq_pad > 0 ? Tq_pad : 1), BH, 32, 32);   // unused when Tq = 0
+        // dK, dV leave as TMA stores: each drain warp stores its 32 key rows, 64 columns per box
+        CUtensorMap tdk, tdv;
+        if (st == OK)
+            st = encode_tmap_3d(&tdk, dk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, Tk, BH, 64, 32);
+        if (st == OK)
+            st = encode_tmap_3d(&tdv, dv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, Tk, BH, 64, 32);
         if (st != OK)
             return st;
         BwdArgs a;
@@ -1103,7 +1156,7 @@ int launch_bwd(const void *q, const void *k, const void *v, const void *o, const
         if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES) != cudaSuccess)
             return ERR_CUDA;
         const int grid = a.units < sms ? a.units : sms;
-        kernel<<<grid, L::NTHREADS, L::SMEM_BYTES, s>>>(tq, tk, tv, tdo, a);
+        kernel<<<grid, L::NTHREADS, L::SMEM_BYTES, s>>>(tq, tk, tv, tdo, tdk, tdv, tacc, a);
         if (cudaGetLastError() != cudaSuccess)
             return ERR_CUDA;
     }

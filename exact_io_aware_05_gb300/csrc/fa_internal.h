@@ -82,6 +82,9 @@ int fp8_quantize_launch(const void *q, const void *k, const void *v, const float
 int fwd_fp8_launch(const void *q8, const void *k8, const void *vt8, const float *qd, const float *kd,
                    const float *vd, void *o, float *lse, int BH, int Tq, int Tk, int d, int causal, float scale,
                    cudaStream_t s);
+// encode_tmap_3d without swizzle (the box is plain row-major in shared memory)
+int encode_tmap_3d_plain(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes,
+                         uint64_t inner, uint64_t rows, uint64_t planes, uint32_t box_inner, uint32_t box_rows);
 // encode_tmap_3d with an explicit row stride in bytes (a multiple of 16)
 int encode_tmap_3d_strided(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes,
                            uint64_t inner, uint64_t rows, uint64_t planes, uint64_t row_stride,
