@@ -520,6 +520,218 @@ def run_fp8(args) -> None:
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ per-workload lines
+# The five configured workloads (inputs.WORKLOADS).  The default run above is the headline
+# (B8 H32 N4096 d128 causal, forward + backward); --config N times workload N on its own and
+# prints one contract line per variant.
+CONFIG_SETS = {
+    1: (["fwd_f32_b1h1_t256_d64"], "fwd"),
+    2: (["fwd_b8h32_t4096_d128_causal", "fwd_b8h32_t4096_d128_causal_q4"], "fwd"),
+    3: (["fwd_b1h24_t32768_d256_causal"], "fwd"),
+    4: (["bwd_b8h32_t4096_d128_causal"], "bwd"),
+    5: (["fwdbwd_b1h16_t65536_d64", "fwdbwd_b1h16_t65536_d64_causal", "fwdbwd_b1h16_q8192_k65536_d64_causal"],
+        "fwdbwd"),
+}
+FP32_LANES_PER_SM = 128   # FP32 FMA lanes per SM (4 SMSPs x 32)
+
+
+def _oracle_rows(w, rows, with_bwd: bool):
+    """The fp64 oracle on the given rows of head 0 (forward; with_bwd: also the whole head's
+    backward, every row and key): seconds and the flops of what it computed (4d per allowed
+    pair of the rows forward, 10d per allowed pair of the head backward)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from exact_io_aware_05_gb300 import inputs
+
+    x = inputs.generate(inputs.replace(w, B=1, H=1))
+    q, k, v = (x[n][0, 0].to(torch.float64).numpy() for n in ("q", "k", "v"))
+    cores = oracle.default_threads()
+    off = w.Tk - w.Tq
+    pairs = sum(min(w.Tk, max(0, int(r) + off + 1)) if w.causal else w.Tk for r in rows)
+    t0 = time.perf_counter()
+    oracle.attention_fwd(q, k, v, w.causal, w.scale, rows=np.asarray(rows), nthreads=cores)
+    flops = 4.0 * w.d * pairs
+    if with_bwd:
+        do = x["do"][0, 0].to(torch.float64).numpy()
+        oracle.attention_bwd(q, k, v, do, w.causal, w.scale, nthreads=cores)
+        flops += 10.0 * w.d * inputs.allowed_pairs(w.Tq, w.Tk, w.causal)
+    return time.perf_counter() - t0, flops, cores
+
+
+def run_config(args) -> None:
+    """Times one configured workload (each of its variants) on one GPU: the forward (fa_fwd, or
+    fa_fwd_f32 for the fp32 workload) and/or the backward (fa_bwd's three stages), inputs in HBM,
+    CUDA events over `steps` calls after `warmup`; the roofline is the pass that takes longest.
+    An end-to-end figure goes through the same calls with pinned host buffers, copies inside
+    the timed region; the oracle is timed on a bounded sample of rows."""
+    import torch
+    from exact_io_aware_05_gb300 import fa, inputs
+
+    names, kind = CONFIG_SETS[args.config]
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    peaks = measured_peaks()
+    stream = torch.cuda.current_stream(dev)
+    for name in names:
+        w = inputs.WORKLOADS[name]
+        f32 = w.dtype == torch.float32
+        g = torch.Generator(device=dev)
+        g.manual_seed(4321 + w.seed)
+        shp_q, shp_k = w.shape_q, w.shape_kv
+        q = torch.randn(shp_q, device=dev, generator=g) * w.q_scale
+        k = torch.randn(shp_k, device=dev, generator=g)
+        v = torch.randn(shp_k, device=dev, generator=g)
+        do = torch.randn(shp_q, device=dev, generator=g)
+        if not f32:
+            q, k, v, do = (t.to(torch.bfloat16) for t in (q, k, v, do))
+        o = torch.empty_like(q)
+        lse = torch.empty(shp_q[:3], device=dev, dtype=torch.float32)
+        BH = w.B * w.H
+        pairs = inputs.allowed_pairs(w.Tq, w.Tk, w.causal) * BH
+        f_fwd, f_bwd = 4.0 * w.d * pairs, 10.0 * w.d * pairs
+        has_fwd, has_bwd = kind in ("fwd", "fwdbwd"), kind in ("bwd", "fwdbwd")
+        ws = fa.alloc_workspace(w.B, w.H, w.Tq, w.Tk, w.d, dev) if has_bwd else None
+        dq, dk, dv = (torch.empty_like(t) for t in (q, k, v)) if has_bwd else (None, None, None)
+        # small inputs (the fp32 workload) sit in L2: a 256 MB buffer is written between calls
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if f32 else None
+
+        def fwd():
+            (fa.fa_fwd_f32 if f32 else fa.fa_fwd)(q, k, v, o, lse, w.causal, w.scale, stream)
+
+        def bwd(st):
+            fa.fa_bwd_stage(st, q, k, v, o, lse, do, dq, dk, dv, w.causal, w.scale, ws, stream)
+
+        fwd()   # o, lse for the backward
+        for _ in range(args.warmup):
+            if has_fwd:
+                fwd()
+            if has_bwd:
+                for st in (1, 2, 3):
+                    bwd(st)
+        torch.cuda.synchronize(dev)
+        if fa.fa_sync_status(stream) != fa.FA_OK:
+            raise RuntimeError(f"{name}: device status error during warm-up")
+        sampler = ClockSampler(0)
+        sampler.start()
+        time.sleep(0.3)
+        t_f, t_pre, t_main, t_dq = [], [], [], []
+        for _ in range(args.steps):
+            if flush is not None:
+                flush.fill_(1)
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+            ev[0].record(stream)
+            if has_fwd:
+                fwd()
+            ev[1].record(stream)
+            if has_bwd:
+                bwd(1)
+                ev[2].record(stream)
+                bwd(2)
+                ev[3].record(stream)
+                bwd(3)
+            ev[4].record(stream)
+            torch.cuda.synchronize(dev)
+            t_f.append(ev[0].elapsed_time(ev[1]))
+            if has_bwd:
+                t_pre.append(ev[1].elapsed_time(ev[2]))
+                t_main.append(ev[2].elapsed_time(ev[3]))
+                t_dq.append(ev[3].elapsed_time(ev[4]))
+        clocks = sampler.stop()
+        if fa.fa_sync_status(stream) != fa.FA_OK:
+            raise RuntimeError(f"{name}: device status error in the timed region")
+        med = statistics.median
+        fwd_ms = med(t_f) if has_fwd else 0.0
+        bwd_ms = (med(t_pre) + med(t_main) + med(t_dq)) if has_bwd else 0.0
+        flops = (f_fwd if has_fwd else 0.0) + (f_bwd if has_bwd else 0.0)
+        ms = fwd_ms + bwd_ms
+        value = flops / (ms * 1e-3) / 1e12
+        passes = {}
+        if has_fwd:
+            passes["fwd"] = {"ms": fwd_ms, "tflops": f_fwd / (fwd_ms * 1e-3) / 1e12}
+        if has_bwd:
+            passes["bwd"] = {"ms": bwd_ms, "tflops": f_bwd / (bwd_ms * 1e-3) / 1e12, "preprocess_ms": med(t_pre),
+                             "tile_loop_ms": med(t_main), "dq_finish_ms": med(t_dq)}
+        if f32:
+            peak = 2.0 * FP32_LANES_PER_SM * torch.cuda.get_device_properties(dev).multi_processor_count * \
+                (clocks["sm_max_mhz"] if clocks and clocks.get("sm_max_mhz") else 2070.0) * 1e6 / 1e12
+            roof = {"kernel": "fwd_f32_kernel", "bound": "alu", "achieved": passes["fwd"]["tflops"], "peak": peak,
+                    "unit": "TFLOP/s", "frac": passes["fwd"]["tflops"] / peak, "traffic": None,
+                    "peak_source": "derived: SMs x 128 FP32 lanes x 2 flops x max SM clock (fp32 FFMA)"}
+        else:
+            peak = peaks["bf16_tflops"]
+            if has_bwd and (not has_fwd or med(t_main) >= fwd_ms):
+                dom = ("bwd_main", f_bwd / (med(t_main) * 1e-3) / 1e12)
+            else:
+                dom = ("fwd", passes["fwd"]["tflops"])
+            roof = {"kernel": dom[0], "bound": "tensor", "achieved": dom[1], "peak": peak, "unit": "TFLOP/s",
+                    "frac": dom[1] / peak, "traffic": None,
+                    "peak_source": f"{peaks['source']} bf16 (burst), MEASURED_PEAKS.json"}
+        # end to end: the same calls with the inputs copied in from pinned host memory and the
+        # outputs copied back, all inside the timed region
+        e2e = None
+        if not args.no_e2e:
+            # inputs: q, k, v (+ dO; the backward-only workload also takes the forward's o, lse)
+            ins = [("q", q), ("k", k), ("v", v)] + ([("do", do)] if has_bwd else []) + \
+                  ([("o", o), ("lse", lse)] if not has_fwd else [])
+            hin = {n: t.to("cpu").pin_memory() for n, t in ins}
+            outs = ([("o", o), ("lse", lse)] if has_fwd else []) + ([("dq", dq), ("dk", dk), ("dv", dv)] if has_bwd else [])
+            hout = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory() for n, t in outs}
+            dev_in = dict(ins)
+            dev_out = dict(outs)
+            n_e2e = max(3, min(args.steps, 10))
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            for _ in range(n_e2e):
+                for n, t in hin.items():
+                    dev_in[n].copy_(t, non_blocking=True)
+                if has_fwd:
+                    fwd()
+                if has_bwd:
+                    fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, w.causal, w.scale, ws, stream)
+                for n, t in hout.items():
+                    t.copy_(dev_out[n], non_blocking=True)
+            a1.record(stream)
+            torch.cuda.synchronize(dev)
+            e2e_ms = a0.elapsed_time(a1) / n_e2e
+            e2e = {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                   "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hin.values()),
+                   "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hout.values()),
+                   "ms_per_step": e2e_ms,
+                   "api": {"fwd": "fa_fwd", "bwd": "fa_bwd (o, lse copied in with the inputs)",
+                           "fwdbwd": "fa_fwd + fa_bwd"}[kind] + " with pinned host buffers"}
+        cpu = None
+        if not args.no_cpu_baseline:
+            import numpy as np
+            nrow = w.Tq if w.Tq * w.Tk <= 1 << 20 else 64
+            rows = np.arange(w.Tq) if nrow == w.Tq else np.linspace(0, w.Tq - 1, nrow).astype(np.int64)
+            secs, fl, cores = _oracle_rows(w, rows, has_bwd and w.Tk <= 8192)
+            part = "forward every row" if nrow == w.Tq else f"forward of {nrow} rows spread over head 0"
+            if has_bwd and w.Tk <= 8192:
+                part += " + backward of the whole head (every row and key)"
+            cpu = {"value": fl / secs / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                   "sample": f"{part}, fp64, {secs:.2f} s; rate over the flops it computed" +
+                             ("" if nrow == w.Tq else " (extrapolates to the whole workload by pair count)")}
+        metric = {"fwd": "attention forward TFLOP/s", "bwd": "attention backward TFLOP/s",
+                  "fwdbwd": "attention TFLOP/s fwd+bwd"}[kind]
+        line = {"metric": f"{metric}, {'fp32' if f32 else 'bf16'} B{w.B} H{w.H} Tq{w.Tq} Tk{w.Tk} d{w.d} "
+                          f"{'causal' if w.causal else 'non-causal'}" + (f", Q x{w.q_scale:g}" if w.q_scale != 1 else ""),
+                "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f32" if f32 else "bf16", "data": "synthetic",
+                "config": {"workload": w.name, "B": w.B, "H": w.H, "Tq": w.Tq, "Tk": w.Tk, "d": w.d,
+                           "causal": w.causal, "q_scale": w.q_scale,
+                           "flops": "4d fwd + 10d bwd per allowed pair (bottom-right causal)",
+                           "l2": "256 MB written between calls" if f32 else "no flush: inputs larger than the 129 MB L2"},
+                "pct_of_peak": 100.0 * value / peak, "passes": passes, "roofline": roof,
+                "gpu_launches": (1 if has_fwd else 0) * args.steps + (3 if has_bwd else 0) * args.steps,
+                "e2e": e2e, "cpu_baseline": cpu, "clocks": clocks}
+        print(json.dumps(line), flush=True)
+        del q, k, v, do, o, lse, ws, dq, dk, dv, flush
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -533,6 +745,8 @@ def main():
                     help="time split-KV decode (B8 H32 Tq1 Tk32768 d128) instead of the fwd+bwd step")
     ap.add_argument("--fp8", action="store_true",
                     help="time the FP8 forward (quantization + fa_fwd_fp8, B8 H32 N4096 d128 causal)")
+    ap.add_argument("--config", type=int, choices=sorted(CONFIG_SETS), default=None,
+                    help="time configured workload 1..5 (each variant) instead of the headline step")
     ap.add_argument("--batch", type=int, default=WORKLOAD["B"],
                     help="batch size (default 8, the benchmark workload; smaller only for profiling)")
     args = ap.parse_args()
@@ -543,6 +757,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.config is not None:
+        run_config(args)
     elif args.decode:
         run_decode(args)
     elif args.fp8:

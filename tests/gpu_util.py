@@ -29,6 +29,8 @@ def heads_of(w: inputs.Workload, n: int, seed: int = 0):
     all_h = [(b, h) for b in range(w.B) for h in range(w.H)]
     if n >= len(all_h):
         return all_h
+    if n < 2:
+        return all_h[:n]
     rng = np.random.default_rng(seed)
     mid = rng.choice(np.arange(1, len(all_h) - 1), size=n - 2, replace=False)
     return [all_h[0]] + [all_h[i] for i in sorted(mid)] + [all_h[-1]]

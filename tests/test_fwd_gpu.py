@@ -28,11 +28,16 @@ def run_fwd(fa, w: inputs.Workload, x=None):
     return x, o, lse
 
 
-def check_heads(w, x, o, lse, heads, rows=None, tol_o=TOL_O_BF16, tol_l=TOL_LSE):
+def check_heads(w, x, o, lse, heads, rows=None, tol_o=TOL_O_BF16, tol_l=TOL_LSE, raw_small=True):
     """Element-wise O and lse against the oracle.  For bf16 outputs the O bound is tol_o on
     top of half a bf16 ulp of the exact value (the output format's own rounding, which by
-    itself exceeds 1e-2 once |O| >= 4); fp32 outputs are held to tol_o outright."""
+    itself exceeds 1e-2 once |O| >= 4); fp32 outputs are held to tol_o outright.  raw_small:
+    bf16 outputs are also held to tol_o outright on every element with |O_ref| < 2, where half
+    an ulp is at most 2^-9.  (Not for inputs with Q scaled up: there the forward's lazy
+    rescale, whose dominant weight is no longer exactly 1 before its bf16 rounding, measured
+    0.011 on those elements.)"""
     worst = (0.0, 0.0, -np.inf)
+    worst_small = 0.0
     for (b, h) in heads:
         q, k, v = (to64(x[n][b, h]) for n in ("q", "k", "v"))
         o_ref, lse_ref = oracle.attention_fwd(q, k, v, w.causal, w.scale, rows=rows)
@@ -41,12 +46,17 @@ def check_heads(w, x, o, lse, heads, rows=None, tol_o=TOL_O_BF16, tol_l=TOL_LSE)
         e_o, e_l, e_ox, dead_ok = fwd_errors(og, lg, o_ref, lse_ref)
         assert dead_ok, f"head {(b, h)}: rows without keys must give O = 0, lse = -inf"
         worst = (max(worst[0], e_o), max(worst[1], e_l), max(worst[2], e_ox))
-    print(f"{w.name}: max|dO|={worst[0]:.3e} (beyond bf16 output rounding {worst[2]:.3e}) "
-          f"max|dlse|={worst[1]:.3e}")
+        small = np.abs(o_ref) < 2
+        if small.any():
+            worst_small = max(worst_small, float(np.abs(og - o_ref)[small].max()))
+    print(f"{w.name}: max|dO|={worst[0]:.3e} (beyond bf16 output rounding {worst[2]:.3e}, "
+          f"where |O| < 2 {worst_small:.3e}) max|dlse|={worst[1]:.3e}")
     if o.dtype == torch.float32:
         assert worst[0] <= tol_o, worst
     else:
         assert worst[2] <= tol_o, worst
+        if raw_small:
+            assert worst_small <= tol_o, ("raw error where |O_ref| < 2", worst_small)
     assert worst[1] <= tol_l, worst
     return worst
 
@@ -89,10 +99,10 @@ def test_fwd_bf16_large_scores(fa):
     O~ rescale path runs."""
     w = inputs.small(1, 4, 640, 640, 128, False, seed=3, q_scale=4.0)
     x, o, lse = run_fwd(fa, w)
-    check_heads(w, x, o, lse, heads_of(w, 4))
+    check_heads(w, x, o, lse, heads_of(w, 4), raw_small=False)
     w = inputs.small(1, 2, 640, 640, 64, True, seed=4, q_scale=6.0)
     x, o, lse = run_fwd(fa, w)
-    check_heads(w, x, o, lse, heads_of(w, 2))
+    check_heads(w, x, o, lse, heads_of(w, 2), raw_small=False)
 
 
 def test_fwd_empty_and_degenerate(fa):
@@ -133,7 +143,7 @@ def test_fwd_empty_and_degenerate(fa):
 def test_fwd_b8h32_t4096_d128(fa, name):
     w = inputs.WORKLOADS[name]
     x, o, lse = run_fwd(fa, w)
-    check_heads(w, x, o, lse, heads_of(w, 8))
+    check_heads(w, x, o, lse, heads_of(w, 8), raw_small=w.q_scale == 1.0)
 
 
 def test_fwd_b1h24_t32768_d256(fa):
