@@ -704,7 +704,7 @@ def run_config(args) -> None:
         cpu = None
         if not args.no_cpu_baseline:
             import numpy as np
-            nrow = w.Tq if w.Tq * w.Tk <= 1 << 20 else 64
+            nrow = w.Tq if w.Tq * w.Tk <= 1 << 24 else 1024
             rows = np.arange(w.Tq) if nrow == w.Tq else np.linspace(0, w.Tq - 1, nrow).astype(np.int64)
             secs, fl, cores = _oracle_rows(w, rows, has_bwd and w.Tk <= 8192)
             part = "forward every row" if nrow == w.Tq else f"forward of {nrow} rows spread over head 0"
