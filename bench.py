@@ -467,6 +467,8 @@ def run_fp8(args) -> None:
     import torch
     from exact_io_aware_05_gb300 import fa, inputs
     w = inputs.WORKLOADS["fwd_fp8_b8h32_t4096_d128_causal"]
+    if args.batch != w.B:   # a smaller batch, for profiling only
+        w = inputs.replace(w, B=args.batch, name=f"fwd_fp8_b{args.batch}h32_t4096_d128_causal (profiling size)")
     torch.cuda.set_device(0)
     g = torch.Generator(device="cuda")
     g.manual_seed(w.seed)
