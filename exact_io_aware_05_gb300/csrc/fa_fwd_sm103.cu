@@ -25,7 +25,7 @@
 //   * warps 1 and 2 (two tiles): one thread each issues the tcgen05.mma and
 //     commits of its tile, S of key block k+1 ahead of P V of block k (P lives
 //     in shared memory, so S may be overwritten once the softmax has read it);
-//     with one tile, warp 1 issues everything;
+//     with one tile, warp 1 issues the S products and warp 2 the P V products;
 //   * one 128-thread softmax warpgroup per query tile (thread = query row =
 //     tensor-memory lane) doing the online softmax and the epilogue; the two
 //     warpgroups run independently;
@@ -281,30 +281,6 @@ __device__ __forceinline__ Plan make_plan(int u, const FwdArgs &a)
                 p.tr1 = tr;
         }
         return p;
-    }
-}
-
-// Job k of a unit -> (query tile t, key block j); first/last: whether this job
-// is the first/last user of K_j (S MMA order) and of V_j (PV MMA order).
-template <int NQ>
-__device__ __forceinline__ void job_of(const Plan &p, int k, int &t, int &j, bool &first, bool &last)
-{
-    if constexpr (NQ == 1) {
-        t = 0;
-        j = k;
-        first = last = true;
-    } else {
-        const int a = min(p.tr0.n, p.tr1.n);
-        if (k < 2 * a) {
-            t = k & 1;
-            j = k >> 1;
-            first = (t == 0);
-            last = (t == 1);
-        } else {
-            t = (p.tr0.n > p.tr1.n) ? 0 : 1;
-            j = a + (k - 2 * a);
-            first = last = true;
-        }
     }
 }
 
@@ -625,42 +601,48 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                 mbar_wait_drain(drain_bar, 0);
             }
             __syncwarp();
-        } else if (NQ == 1 && warp == 1) {
-            // ------------------------------------------------ MMA issuer (one query tile)
+        } else if (NQ == 1 && (warp == 1 || warp == 2)) {
+            // ------------------------------------------------ MMA issuers (one query tile)
+            // Warp 1 issues the S products and warp 2 the P V products, so that neither waits
+            // behind the other's barriers: S(k+2) goes out as soon as P V(k) has read P(k) from
+            // the S buffer that it overwrites, and P V(k) as soon as the softmax has written
+            // P(k).  A tcgen05.mma blocks its issuing thread while the tensor core's queue is
+            // full, so with one issuer every wait of one product stalled the other's issue.
+            // Both warps locate their tiles in the K/V ring by the producer's load order of the
+            // unit, S(0), S(1), PV(0), S(2), PV(1), ...: S(k) is load k ? 2k - 1 : 0 and P V(k)
+            // is load min(J, k + 2) + k.
             if (lane == 0) {
-                uint32_t ld = 0, kg = 0, q_seen = 0;
-                uint32_t epi[2] = {0, 0};
-                for (int pass = 0, u = snake_unit<!MASKED>(0); u < a.units; u = snake_unit<!MASKED>(++pass)) {
+                const bool s_side = warp == 1;
+                uint32_t base = 0, kg = 0, q_seen = 0, epi = 0;
+                bool ok = true;
+                for (int pass = 0, u = snake_unit<!MASKED>(0); u < a.units && ok; u = snake_unit<!MASKED>(++pass)) {
                     const Plan p = make_plan<D, MASKED>(u, a);
-                    if (p.J == 0)
+                    const int J = p.J;
+                    if (J == 0)
                         continue;
-                    if (!mbar_wait<INL>(bar(L::B_QFULL), q_seen & 1, ctx, SITE_M_QFULL))
-                        break;
-                    ++q_seen;
-                    uint32_t kslot = 0, vslot = 0;
-                    auto acquire = [&](uint32_t &slot) -> bool {
-                        slot = ld % NSLOT;
-                        const bool ok = mbar_wait<INL>(bar(L::B_FULL + slot), (ld / NSLOT) & 1, ctx, SITE_M_FULL);
-                        ++ld;
-                        return ok;
-                    };
-                    const bool ok = walk_ops(
-                        p.J,
-                        [&](int k) -> bool {
-                            int t, j;
-                            bool first, last;
-                            job_of<NQ>(p, k, t, j, first, last);
-                            if (first && !acquire(kslot))
-                                return false;
-                            const uint32_t b = (kg + k) & 1;
-                            // S overwrites the columns that held P of job (kg + k - 2): that PV
-                            // must have finished reading them
-                            const uint32_t g = kg + k;
-                            if (g >= 2 && !mbar_wait<INL>(bar(L::B_PREAD + b), ((g - 2) >> 1) & 1, ctx, SITE_M_PREAD))
-                                return false;
+                    if (s_side) {
+                        if (!mbar_wait<INL>(bar(L::B_QFULL), q_seen & 1, ctx, SITE_M_QFULL))
+                            break;
+                        ++q_seen;
+                    }
+                    for (int k = 0; k < J && ok; ++k) {
+                        const uint32_t g = kg + k, b = g & 1;
+                        const uint32_t n = base + (uint32_t)(s_side ? (k ? 2 * k - 1 : 0) : min(J, k + 2) + k);
+                        const uint32_t slot = n % NSLOT;
+                        if (!mbar_wait<INL>(bar(L::B_FULL + slot), (n / NSLOT) & 1, ctx, SITE_M_FULL)) {
+                            ok = false;
+                            break;
+                        }
+                        if (s_side) {
+                            // S(g) overwrites the columns that held P(g - 2): P V(g - 2) must have
+                            // finished reading them
+                            if (g >= 2 && !mbar_wait<INL>(bar(L::B_PREAD + b), ((g - 2) >> 1) & 1, ctx, SITE_M_PREAD)) {
+                                ok = false;
+                                break;
+                            }
                             tc_fence_after();
-                            const uint64_t qd = sdesc_sw128(sbase + L::OFF_Q + t * L::Q_TILE, 16, 1024);
-                            const uint64_t kd = sdesc_sw128(sbase + L::OFF_SLOT + kslot * L::KV_TILE, 16, 1024);
+                            const uint64_t qd = sdesc_sw128(sbase + L::OFF_Q, 16, 1024);
+                            const uint64_t kd = sdesc_sw128(sbase + L::OFF_SLOT + slot * L::KV_TILE, 16, 1024);
 #pragma unroll
                             for (int kk = 0; kk < D / 16; ++kk) {   // 16 bf16 = 32 bytes along K
                                 const uint32_t off = ((kk >> 2) * L::Q_CHUNK + (kk & 3) * 32) >> 4;
@@ -668,54 +650,48 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                                 mma_ss(tmem + L::S_COL + b * BC, qd + off, kd + offk, L::IDESC_S, kk > 0 ? 1u : 0u);
                             }
                             tc_commit(bar(L::B_SFULL + b));
-                            if (last)
-                                tc_commit(bar(L::B_EMPTY + kslot));
-                            if (k == p.J - 1)
+                            tc_commit(bar(L::B_EMPTY + slot));
+                            if (k == J - 1)
                                 tc_commit(bar(L::B_QEMPTY));
-                            return true;
-                        },
-                        [&](int k) -> bool {
-                            int t, j;
-                            bool first, last;
-                            job_of<NQ>(p, k, t, j, first, last);
-                            if (first && !acquire(vslot))
-                                return false;
-                            const uint32_t b = (kg + k) & 1;
-                            if (!mbar_wait<INL>(bar(L::B_PFULL + b), ((kg + k) >> 1) & 1, ctx, SITE_M_PFULL))
-                                return false;
-                            if (j == 0 && epi[t] > 0 &&
-                                !mbar_wait<INL>(bar(L::B_OEMPTY + t), (epi[t] - 1) & 1, ctx, SITE_M_OEMPTY))
-                                return false;
+                        } else {
+                            if (!mbar_wait<INL>(bar(L::B_PFULL + b), (g >> 1) & 1, ctx, SITE_M_PFULL)) {
+                                ok = false;
+                                break;
+                            }
+                            if (k == 0 && epi > 0 &&
+                                !mbar_wait<INL>(bar(L::B_OEMPTY), (epi - 1) & 1, ctx, SITE_M_OEMPTY)) {
+                                ok = false;
+                                break;
+                            }
                             tc_fence_after();
-                            const uint64_t vd = sdesc_sw128(sbase + L::OFF_SLOT + vslot * L::KV_TILE, L::KV_CHUNK, 1024);
-                            if (j == 0) {
+                            const uint64_t vd = sdesc_sw128(sbase + L::OFF_SLOT + slot * L::KV_TILE, L::KV_CHUNK, 1024);
+                            if (k == 0) {
 #pragma unroll
                                 for (int kk = 0; kk < BC / 16; ++kk)
-                                    mma_ts(tmem + L::O_COL + t * D, tmem + L::S_COL + b * BC + kk * 8,
+                                    mma_ts(tmem + L::O_COL, tmem + L::S_COL + b * BC + kk * 8,
                                            vd + ((kk * 16 * 128) >> 4), L::IDESC_PV, kk > 0 ? 1u : 0u);
                             } else {
 #pragma unroll
                                 for (int kk = 0; kk < BC / 16; ++kk)
-                                    mma_ts(tmem + L::O_COL + t * D, tmem + L::S_COL + b * BC + kk * 8,
+                                    mma_ts(tmem + L::O_COL, tmem + L::S_COL + b * BC + kk * 8,
                                            vd + ((kk * 16 * 128) >> 4), L::IDESC_PV, 1u);
                             }
-                            tc_commit(bar(L::B_ODONE + t));
+                            tc_commit(bar(L::B_ODONE));
                             tc_commit(bar(L::B_PREAD + b));
-                            if (last)
-                                tc_commit(bar(L::B_EMPTY + vslot));
-                            if (j == tile_of(p, t).n - 1) {   // last PV of this tile in the unit
-                                tc_commit(bar(L::B_OFINAL + t));
-                                ++epi[t];
+                            tc_commit(bar(L::B_EMPTY + slot));
+                            if (k == J - 1) {   // last P V of the unit
+                                tc_commit(bar(L::B_OFINAL));
+                                ++epi;
                             }
-                            return true;
-                        });
-                    if (!ok)
-                        break;
-                    kg += p.J;
+                        }
+                    }
+                    base += 2u * (uint32_t)J;
+                    kg += (uint32_t)J;
                 }
-                // drain: all issued MMAs complete before tensor memory is released
-                tc_commit(bar(L::B_DRAIN));
-                mbar_wait_drain(bar(L::B_DRAIN), 0);
+                // drain: all MMAs this thread issued complete before tensor memory is released
+                const uint32_t drain_bar = bar(s_side ? L::B_DRAIN : L::B_DRAIN1);
+                tc_commit(drain_bar);
+                mbar_wait_drain(drain_bar, 0);
             }
             __syncwarp();
         }
