@@ -99,16 +99,20 @@ struct FwdLayout {
     static constexpr int NSLOT = PSM ? (NSLOT_FIT < 8 ? NSLOT_FIT : 8) : (F8 ? 8 : C::NSLOT);
     static_assert(NSLOT >= 3, "K/V ring depth");
     static constexpr int OFF_BAR = OFF_SLOT + NSLOT * KV_TILE;
+    // S buffers in tensor memory: one per tile with two tiles; with one tile, three that
+    // the key blocks take in turn (P goes back over S there, so S of block k + 3 waits
+    // only for P V of block k)
+    static constexpr int NSB = NQ == 1 ? 3 : 2;
     // barrier indices
     static constexpr int B_FULL = 0, B_EMPTY = NSLOT, B_QFULL = 2 * NSLOT, B_QEMPTY = 2 * NSLOT + 1,
-                         B_SFULL = 2 * NSLOT + 2, B_PFULL = 2 * NSLOT + 4, B_ODONE = 2 * NSLOT + 6,
-                         B_OEMPTY = 2 * NSLOT + 8, B_DRAIN = 2 * NSLOT + 10, B_PREAD = 2 * NSLOT + 11,
-                         B_OFINAL = 2 * NSLOT + 13, B_DRAIN1 = 2 * NSLOT + 15, B_SFREE = 2 * NSLOT + 16,
-                         NBAR = 2 * NSLOT + 18;
+                         B_SFULL = 2 * NSLOT + 2, B_PFULL = B_SFULL + NSB, B_ODONE = B_PFULL + NSB,
+                         B_OEMPTY = B_ODONE + 2, B_DRAIN = B_OEMPTY + 2, B_PREAD = B_DRAIN + 1,
+                         B_OFINAL = B_PREAD + NSB, B_DRAIN1 = B_OFINAL + 2, B_SFREE = B_DRAIN1 + 1,
+                         NBAR = B_SFREE + 2;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;   // tmem base (u32), abort flag (int)
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1024-byte alignment
     static constexpr int S_COL = 0;                  // S buffer b at columns [b*BC, (b+1)*BC)
-    static constexpr int O_COL = 2 * BC;             // O~ of tile t at [O_COL + t*D, +D)
+    static constexpr int O_COL = NSB * BC;           // O~ of tile t at [O_COL + t*D, +D)
     static constexpr int TMEM_COLS = 512;
     static constexpr int NTHREADS = 128 + NQ * 128;
     static_assert(O_COL + NQ * D <= TMEM_COLS, "tensor memory budget");
@@ -356,14 +360,15 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
         }
         mbar_init(bar(L::B_QFULL), 1);
         mbar_init(bar(L::B_QEMPTY), NQ);
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < L::NSB; ++b) {
             mbar_init(bar(L::B_SFULL + b), 1);
             mbar_init(bar(L::B_PFULL + b), 128);
+            mbar_init(bar(L::B_PREAD + b), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
             mbar_init(bar(L::B_ODONE + b), 1);
             mbar_init(bar(L::B_OEMPTY + b), 128);
         }
-        mbar_init(bar(L::B_PREAD), 1);
-        mbar_init(bar(L::B_PREAD + 1), 1);
         mbar_init(bar(L::B_OFINAL), 1);
         mbar_init(bar(L::B_OFINAL + 1), 1);
         mbar_init(bar(L::B_DRAIN), 1);
@@ -626,7 +631,7 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                         ++q_seen;
                     }
                     for (int k = 0; k < J && ok; ++k) {
-                        const uint32_t g = kg + k, b = g & 1;
+                        const uint32_t g = kg + k, b = g % L::NSB;
                         const uint32_t n = base + (uint32_t)(s_side ? (k ? 2 * k - 1 : 0) : min(J, k + 2) + k);
                         const uint32_t slot = n % NSLOT;
                         if (!mbar_wait<INL>(bar(L::B_FULL + slot), (n / NSLOT) & 1, ctx, SITE_M_FULL)) {
@@ -634,9 +639,10 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                             break;
                         }
                         if (s_side) {
-                            // S(g) overwrites the columns that held P(g - 2): P V(g - 2) must have
-                            // finished reading them
-                            if (g >= 2 && !mbar_wait<INL>(bar(L::B_PREAD + b), ((g - 2) >> 1) & 1, ctx, SITE_M_PREAD)) {
+                            // S(g) overwrites the columns that held P(g - NSB): P V(g - NSB) must
+                            // have finished reading them
+                            if (g >= (uint32_t)L::NSB &&
+                                !mbar_wait<INL>(bar(L::B_PREAD + b), (g / L::NSB - 1) & 1, ctx, SITE_M_PREAD)) {
                                 ok = false;
                                 break;
                             }
@@ -654,7 +660,7 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                             if (k == J - 1)
                                 tc_commit(bar(L::B_QEMPTY));
                         } else {
-                            if (!mbar_wait<INL>(bar(L::B_PFULL + b), (g >> 1) & 1, ctx, SITE_M_PFULL)) {
+                            if (!mbar_wait<INL>(bar(L::B_PFULL + b), (g / L::NSB) & 1, ctx, SITE_M_PFULL)) {
                                 ok = false;
                                 break;
                             }
@@ -676,7 +682,9 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                                     mma_ts(tmem + L::O_COL, tmem + L::S_COL + b * BC + kk * 8,
                                            vd + ((kk * 16 * 128) >> 4), L::IDESC_PV, 1u);
                             }
-                            tc_commit(bar(L::B_ODONE));
+                            // O~ holds P V(g): the softmax may be up to NSB jobs ahead, so the
+                            // signal alternates between two barriers to stay within one phase
+                            tc_commit(bar(L::B_ODONE + (g & 1)));
                             tc_commit(bar(L::B_PREAD + b));
                             tc_commit(bar(L::B_EMPTY + slot));
                             if (k == J - 1) {   // last P V of the unit
@@ -733,10 +741,10 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
             // jj: job index of this tile; j: the KV block it visits
             for (int jj = 0, j = MASKED ? me.first : 0; jj < me.n && ok;
                  ++jj, j = MASKED ? next_active<BC>(me, j + 1) : jj) {
-                // two tiles: S buffer t, one phase per job of this tile; one tile: the two
-                // S buffers alternate between consecutive jobs
-                const uint32_t b = NQ == 2 ? (uint32_t)t : (pv & 1);
-                const uint32_t ph = NQ == 2 ? (pv & 1) : ((pv >> 1) & 1);
+                // two tiles: S buffer t, one phase per job of this tile; one tile: the NSB
+                // S buffers take consecutive jobs in turn
+                const uint32_t b = NQ == 2 ? (uint32_t)t : (pv % L::NSB);
+                const uint32_t ph = NQ == 2 ? (pv & 1) : ((pv / L::NSB) & 1);
                 if (!mbar_wait_warp<INL>(bar(L::B_SFULL + b), ph, ctx, SITE_S_SFULL)) {
                     ok = false;
                     break;
@@ -893,7 +901,8 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                 if (__any_sync(0xffffffffu, resc)) {
                     // O~ must hold the previous PV of this tile before it is rescaled (two tiles:
                     // waited for above)
-                    if (!L::PSM && !mbar_wait_warp<INL>(bar(L::B_ODONE + t), (pv - 1) & 1, ctx, SITE_S_ODONE)) {
+                    if (!L::PSM &&
+                        !mbar_wait_warp<INL>(bar(L::B_ODONE + ((pv - 1) & 1)), ((pv - 1) >> 1) & 1, ctx, SITE_S_ODONE)) {
                         ok = false;
                         break;
                     }
