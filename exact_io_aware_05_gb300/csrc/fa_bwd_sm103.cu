@@ -213,20 +213,6 @@ __device__ __forceinline__ void fence_proxy_async_smem()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Bulk reduce-add of `bytes` from shared memory into global memory by the TMA engine
-// (fp32 add, or 32-bit integer add for the fixed-point accumulator), in a bulk group.
-__device__ __forceinline__ void bulk_reduce_add_f32(void *dst, uint32_t src, uint32_t bytes)
-{
-    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(dst), "r"(src),
-                 "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_reduce_add_u32(void *dst, uint32_t src, uint32_t bytes)
-{
-    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.u32 [%0], [%1], %2;" ::"l"(dst), "r"(src),
-                 "r"(bytes)
-                 : "memory");
-}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // at most one bulk group of this thread still reading shared memory
 __device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
@@ -712,9 +698,7 @@ __global__ void __launch_bounds__(512, 1)
                 }
                 tc_fence_after();
                 const int qb = qi * BQ;
-                float *acc = a.dq_acc + ((size_t)x.bh * a.Tq_pad + qb) * D;
                 const float dsc = a.det_bound ? det_block_scale(a.det_bound[((size_t)x.bh * a.Tq_pad + qb) / BQ]) : 0.f;
-                int *iacc = reinterpret_cast<int *>(acc);
                 if constexpr (L::DQ_ALIAS) {
                     // lane = feature, column = query.  The whole tile is read into registers
                     // first, so the columns go back to the MMA at once; then four chunks of 32
@@ -766,10 +750,12 @@ __global__ void __launch_bounds__(512, 1)
                     stage_chunk(vd, 3);
                 } else {
                     // lane = query, column = feature: each drain warp holds the 32 queries of its
-                    // TMEM lanes, writes them into its own staging buffer ([query][feature], a
-                    // 256-byte row per thread) and its lane 0 hands the 8 KB to the TMA engine as a
-                    // bulk reduce-add.  The buffer's previous reduce-add (one block earlier) has
-                    // long finished reading it; lane 0 confirms before the warp writes.
+                    // TMEM lanes and writes them into its own staging buffer as two boxes of 32
+                    // queries x 32 features with the 128-byte swizzle (16-byte unit u of row r at
+                    // unit u ^ (r mod 8)), so that the 32 lanes' stores of one unit fall in distinct
+                    // banks; its lane 0 hands each box to the TMA engine as a tensor reduce-add.
+                    // The buffer's previous reduce-adds (one block earlier) have long finished
+                    // reading it; lane 0 confirms before the warp writes.
                     uint32_t v[L::DQ_COLS / 32][32];
 #pragma unroll
                     for (int c = 0; c < L::DQ_COLS / 32; ++c)
@@ -782,7 +768,9 @@ __global__ void __launch_bounds__(512, 1)
                     if (lane == 0)
                         bulk_wait_read_all();
                     __syncwarp();
-                    uint8_t *srow = smem + L::OFF_STG + quarter * L::STG_BYTES + lane * (D * 4);
+                    static_assert(L::DQ_COLS / 32 * 4096 == L::STG_BYTES, "two 4 KB boxes per drain warp");
+                    const uint32_t wbox = L::OFF_STG + quarter * L::STG_BYTES;   // 1024-byte aligned
+                    uint8_t *srow = smem + wbox + lane * 128;
 #pragma unroll
                     for (int c = 0; c < L::DQ_COLS / 32; ++c) {
                         uint32_t w[32];
@@ -791,18 +779,15 @@ __global__ void __launch_bounds__(512, 1)
                             w[e] = a.det_bound ? (uint32_t)__float2int_rn(__uint_as_float(v[c][e]) * dsc) : v[c][e];
 #pragma unroll
                         for (int u4 = 0; u4 < 8; ++u4)
-                            *reinterpret_cast<uint4 *>(srow + c * 128 + u4 * 16) =
+                            *reinterpret_cast<uint4 *>(srow + c * 4096 + ((u4 ^ (lane & 7)) << 4)) =
                                 make_uint4(w[4 * u4], w[4 * u4 + 1], w[4 * u4 + 2], w[4 * u4 + 3]);
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        const uint32_t src = sbase + L::OFF_STG + quarter * L::STG_BYTES;
-                        const size_t off = (size_t)quarter * 32 * D;
-                        if (a.det_bound)
-                            bulk_reduce_add_u32(iacc + off, src, L::STG_BYTES);
-                        else
-                            bulk_reduce_add_f32(acc + off, src, L::STG_BYTES);
+#pragma unroll
+                        for (int c = 0; c < L::DQ_COLS / 32; ++c)
+                            tma_reduce_add_3d(&tm_acc, sbase + wbox + c * 4096, c * 32, qb + (int)quarter * 32, x.bh);
                         bulk_commit();
                     }
                 }
@@ -1104,11 +1089,16 @@ int launch_bwd(const void *q, const void *k, const void *v, const void *o, const
         if (st == OK)
             st = encode_tmap_3d(&tdo, Tq > 0 ? dO : k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, tq_rows, BH, 64, BQ);
         // dQ accumulator ([BH][Tq_pad][D], fp32 or, deterministic, int32): each drain warp adds
-        // boxes of its 32 features x 32 queries (d = 128)
+        // boxes of 32 features x 32 queries, staged plain (d = 128: a warp writes one query's 32
+        // features per instruction) or with the 128-byte swizzle (d = 64: a thread writes its
+        // query's row)
         CUtensorMap tacc;
-        if (st == OK)
-            st = encode_tmap_3d_plain(&tacc, ws.dq_acc, det ? CU_TENSOR_MAP_DATA_TYPE_INT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                                      4, D, (uint64_t)(Tq_pad > 0 ? Tq_pad : 1), BH, 32, 32);   // unused when Tq = 0
+        if (st == OK) {
+            const CUtensorMapDataType at = det ? CU_TENSOR_MAP_DATA_TYPE_INT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+            const uint64_t arows = (uint64_t)(Tq_pad > 0 ? Tq_pad : 1);   // unused when Tq = 0
+            st = L::DQ_ALIAS ? encode_tmap_3d_plain(&tacc, ws.dq_acc, at, 4, D, arows, BH, 32, 32)
+                             : encode_tmap_3d(&tacc, ws.dq_acc, at, 4, D, arows, BH, 32, 32);
+        }
         // dK, dV leave as TMA stores: each drain warp stores its 32 key rows, 64 columns per box
         CUtensorMap tdk, tdv;
         if (st == OK)
