@@ -139,10 +139,25 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
 // can see different outcomes when a wait gives up: one lane may see the phase complete
 // while another, polling a moment earlier, has seen the abort flag.  Every lane of the
 // warp must call it.
-template <bool kInline = false>
+//
+// kLane0: lane 0 alone polls, its outcome goes to every lane, and the warp barrier that
+// follows orders the other lanes' reads after lane 0's observation of the phase.  Where
+// the tensor core's operand reads keep shared memory busy (the one-tile forward), 32
+// lanes polling one barrier word take wavefronts from them; elsewhere the vote measured
+// faster.
+template <bool kInline = false, bool kLane0 = false>
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const WaitCtx &ctx, int site)
 {
-    return __all_sync(0xffffffffu, mbar_wait<kInline>(bar, parity, ctx, site));
+    if constexpr (kLane0) {
+        uint32_t ok = 0;
+        if ((threadIdx.x & 31u) == 0)
+            ok = mbar_wait<kInline>(bar, parity, ctx, site) ? 1u : 0u;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        __syncwarp();
+        return ok != 0;
+    } else {
+        return __all_sync(0xffffffffu, mbar_wait<kInline>(bar, parity, ctx, site));
+    }
 }
 
 // Limit of the teardown waits below, fixed and independent of the main waits' limit

@@ -341,6 +341,7 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
     static_assert(!(F8 && MASKED), "the FP8 forward takes no window or block mask");
     constexpr int BC = L::BC, NQ = L::NQ, NSLOT = L::NSLOT;
     constexpr bool INL = NQ == 2;   // register split below: bounded waits inlined (no calls)
+    constexpr bool L1 = NQ == 1;    // softmax waits: lane 0 polls for the warp (see mbar_wait_warp)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -745,7 +746,7 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                 // S buffers take consecutive jobs in turn
                 const uint32_t b = NQ == 2 ? (uint32_t)t : (pv % L::NSB);
                 const uint32_t ph = NQ == 2 ? (pv & 1) : ((pv / L::NSB) & 1);
-                if (!mbar_wait_warp<INL>(bar(L::B_SFULL + b), ph, ctx, SITE_S_SFULL)) {
+                if (!mbar_wait_warp<INL, L1>(bar(L::B_SFULL + b), ph, ctx, SITE_S_SFULL)) {
                     ok = false;
                     break;
                 }
@@ -902,7 +903,7 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                     // O~ must hold the previous PV of this tile before it is rescaled (two tiles:
                     // waited for above)
                     if (!L::PSM &&
-                        !mbar_wait_warp<INL>(bar(L::B_ODONE + ((pv - 1) & 1)), ((pv - 1) >> 1) & 1, ctx, SITE_S_ODONE)) {
+                        !mbar_wait_warp<INL, L1>(bar(L::B_ODONE + ((pv - 1) & 1)), ((pv - 1) >> 1) & 1, ctx, SITE_S_ODONE)) {
                         ok = false;
                         break;
                     }
@@ -943,7 +944,7 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
             // epilogue: O = O~ / l, lse = c m + ln l.  With one tile the softmax can be up
             // to two PVs ahead of the tensor core here, too far for a parity wait on the
             // per-PV barrier; the per-unit barrier completes exactly once per epilogue.
-            if (!mbar_wait_warp<INL>(bar(L::B_OFINAL + t), ep & 1, ctx, SITE_S_EPI))
+            if (!mbar_wait_warp<INL, L1>(bar(L::B_OFINAL + t), ep & 1, ctx, SITE_S_EPI))
                 break;
             ++ep;
             tc_fence_after();
