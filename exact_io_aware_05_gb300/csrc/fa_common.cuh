@@ -61,16 +61,30 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
+// kHintNs > 0: the thread may stay suspended in the instruction up to about that many
+// nanoseconds while the phase is incomplete (it resumes as soon as the phase completes),
+// instead of the hardware's own limit; fewer polls of the barrier word.
+template <uint32_t kHintNs = 0>
 __device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
+    if constexpr (kHintNs == 0) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity), "r"(kHintNs)
+            : "memory");
+    }
     return ok;
 }
 
@@ -98,11 +112,12 @@ struct WaitCtx {
 // (returns false) when another role of the CTA has aborted, or after
 // ctx.timeout_ns, in which case it raises the abort flag and records
 // (site << 8 | FA_ERR_TIMEOUT) in the status word.  Never traps.
+template <uint32_t kHintNs = 0>
 __device__ __forceinline__ bool mbar_wait_loop(uint32_t bar, uint32_t parity, const WaitCtx &ctx, int site)
 {
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity))
+        if (mbar_try_wait<kHintNs>(bar, parity))
             return true;
         if (*ctx.abort)
             return false;
@@ -115,22 +130,24 @@ __device__ __forceinline__ bool mbar_wait_loop(uint32_t bar, uint32_t parity, co
     }
 }
 
+template <uint32_t kHintNs>
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitCtx &ctx, int site)
 {
-    return mbar_wait_loop(bar, parity, ctx, site);
+    return mbar_wait_loop<kHintNs>(bar, parity, ctx, site);
 }
 
 // kInline: the slow path inlined instead of called.  Code that runs under a
-// setmaxnreg register count cannot call out-of-line functions.
-template <bool kInline = false>
+// setmaxnreg register count cannot call out-of-line functions.  kHintNs: see
+// mbar_try_wait.
+template <bool kInline = false, uint32_t kHintNs = 0>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtx &ctx, int site)
 {
-    if (mbar_try_wait(bar, parity))
+    if (mbar_try_wait<kHintNs>(bar, parity))
         return true;
     if constexpr (kInline)
-        return mbar_wait_loop(bar, parity, ctx, site);
+        return mbar_wait_loop<kHintNs>(bar, parity, ctx, site);
     else
-        return mbar_wait_slow(bar, parity, ctx, site);
+        return mbar_wait_slow<kHintNs>(bar, parity, ctx, site);
 }
 
 // The same wait for roles whose warps run warp-collective instructions (tensor-memory
@@ -145,18 +162,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
 // the tensor core's operand reads keep shared memory busy (the one-tile forward), 32
 // lanes polling one barrier word take wavefronts from them; elsewhere the vote measured
 // faster.
-template <bool kInline = false, bool kLane0 = false>
+template <bool kInline = false, bool kLane0 = false, uint32_t kHintNs = 0>
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const WaitCtx &ctx, int site)
 {
     if constexpr (kLane0) {
         uint32_t ok = 0;
         if ((threadIdx.x & 31u) == 0)
-            ok = mbar_wait<kInline>(bar, parity, ctx, site) ? 1u : 0u;
+            ok = mbar_wait<kInline, kHintNs>(bar, parity, ctx, site) ? 1u : 0u;
         ok = __shfl_sync(0xffffffffu, ok, 0);
         __syncwarp();
         return ok != 0;
     } else {
-        return __all_sync(0xffffffffu, mbar_wait<kInline>(bar, parity, ctx, site));
+        return __all_sync(0xffffffffu, mbar_wait<kInline, kHintNs>(bar, parity, ctx, site));
     }
 }
 

@@ -342,6 +342,7 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
     constexpr int BC = L::BC, NQ = L::NQ, NSLOT = L::NSLOT;
     constexpr bool INL = NQ == 2;   // register split below: bounded waits inlined (no calls)
     constexpr bool L1 = NQ == 1;    // softmax waits: lane 0 polls for the warp (see mbar_wait_warp)
+    constexpr uint32_t HN = NQ == 1 ? 4000u : 0u;   // one tile: waits suspend up to 4 us per poll
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -409,7 +410,7 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                     const Plan p = make_plan<D, MASKED>(u, a);
                     if (p.J == 0)
                         continue;
-                    if (n_q > 0 && !mbar_wait<INL>(bar(L::B_QEMPTY), (n_q - 1) & 1, ctx, SITE_P_QEMPTY))
+                    if (n_q > 0 && !mbar_wait<INL, HN>(bar(L::B_QEMPTY), (n_q - 1) & 1, ctx, SITE_P_QEMPTY))
                         break;
                     uint32_t qbytes = 0;
                     for (int t = 0; t < NQ; ++t)
@@ -424,7 +425,7 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                     auto load = [&](const CUtensorMap *map, int j) -> bool {
                         const uint32_t slot = n_loads % NSLOT;
                         if (n_loads >= NSLOT &&
-                            !mbar_wait<INL>(bar(L::B_EMPTY + slot), ((n_loads / NSLOT) - 1) & 1, ctx, SITE_P_EMPTY))
+                            !mbar_wait<INL, HN>(bar(L::B_EMPTY + slot), ((n_loads / NSLOT) - 1) & 1, ctx, SITE_P_EMPTY))
                             return false;
                         mbar_arrive_expect_tx(bar(L::B_FULL + slot), L::KV_TILE);
                         const uint32_t dst = sbase + L::OFF_SLOT + slot * L::KV_TILE;
@@ -499,7 +500,7 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                     const Plan p = make_plan<D, MASKED>(u, a);
                     if (p.J == 0)
                         continue;
-                    if (!mbar_wait<INL>(bar(L::B_QFULL), q_seen & 1, ctx, SITE_M_QFULL))
+                    if (!mbar_wait<INL, HN>(bar(L::B_QFULL), q_seen & 1, ctx, SITE_M_QFULL))
                         break;
                     ++q_seen;
                     const TileRange me = tile_of(p, t);
@@ -508,7 +509,7 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                     auto mine = [&](int j) { return MASKED ? tile_active<BC>(me, j) : j < me.n; };
                     auto acquire = [&](uint32_t &slot) -> bool {
                         slot = ld % NSLOT;
-                        const bool r = mbar_wait<INL>(bar(L::B_FULL + slot), (ld / NSLOT) & 1, ctx, SITE_M_FULL);
+                        const bool r = mbar_wait<INL, HN>(bar(L::B_FULL + slot), (ld / NSLOT) & 1, ctx, SITE_M_FULL);
                         ++ld;
                         return r;
                     };
@@ -527,7 +528,7 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                                 return true;
                             }
                             // S_t is overwritten once the softmax has read the previous S_t
-                            if (sn > 0 && !mbar_wait<INL>(bar(L::B_SFREE + t), (sn - 1) & 1, ctx, SITE_M_PREAD))
+                            if (sn > 0 && !mbar_wait<INL, HN>(bar(L::B_SFREE + t), (sn - 1) & 1, ctx, SITE_M_PREAD))
                                 return false;
                             tc_fence_after();
                             // descriptors: bases once, then compile-time offsets (address field in
@@ -566,11 +567,11 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                                 mbar_arrive(bar(L::B_EMPTY + vs));
                                 return true;
                             }
-                            if (!mbar_wait<INL>(bar(L::B_PFULL + t), pvn & 1, ctx, SITE_M_PFULL))
+                            if (!mbar_wait<INL, HN>(bar(L::B_PFULL + t), pvn & 1, ctx, SITE_M_PFULL))
                                 return false;
                             const bool first = j == (MASKED ? me.first : 0);
                             if (first && epi > 0 &&
-                                !mbar_wait<INL>(bar(L::B_OEMPTY + t), (epi - 1) & 1, ctx, SITE_M_OEMPTY))
+                                !mbar_wait<INL, HN>(bar(L::B_OEMPTY + t), (epi - 1) & 1, ctx, SITE_M_OEMPTY))
                                 return false;
                             tc_fence_after();
                             // P: K-major, 32 bytes of keys per step; V^T (FP8) K-major likewise, bf16 V
@@ -627,7 +628,7 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                     if (J == 0)
                         continue;
                     if (s_side) {
-                        if (!mbar_wait<INL>(bar(L::B_QFULL), q_seen & 1, ctx, SITE_M_QFULL))
+                        if (!mbar_wait<INL, HN>(bar(L::B_QFULL), q_seen & 1, ctx, SITE_M_QFULL))
                             break;
                         ++q_seen;
                     }
@@ -635,7 +636,7 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                         const uint32_t g = kg + k, b = g % L::NSB;
                         const uint32_t n = base + (uint32_t)(s_side ? (k ? 2 * k - 1 : 0) : min(J, k + 2) + k);
                         const uint32_t slot = n % NSLOT;
-                        if (!mbar_wait<INL>(bar(L::B_FULL + slot), (n / NSLOT) & 1, ctx, SITE_M_FULL)) {
+                        if (!mbar_wait<INL, HN>(bar(L::B_FULL + slot), (n / NSLOT) & 1, ctx, SITE_M_FULL)) {
                             ok = false;
                             break;
                         }
@@ -643,7 +644,7 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                             // S(g) overwrites the columns that held P(g - NSB): P V(g - NSB) must
                             // have finished reading them
                             if (g >= (uint32_t)L::NSB &&
-                                !mbar_wait<INL>(bar(L::B_PREAD + b), (g / L::NSB - 1) & 1, ctx, SITE_M_PREAD)) {
+                                !mbar_wait<INL, HN>(bar(L::B_PREAD + b), (g / L::NSB - 1) & 1, ctx, SITE_M_PREAD)) {
                                 ok = false;
                                 break;
                             }
@@ -661,12 +662,12 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                             if (k == J - 1)
                                 tc_commit(bar(L::B_QEMPTY));
                         } else {
-                            if (!mbar_wait<INL>(bar(L::B_PFULL + b), (g / L::NSB) & 1, ctx, SITE_M_PFULL)) {
+                            if (!mbar_wait<INL, HN>(bar(L::B_PFULL + b), (g / L::NSB) & 1, ctx, SITE_M_PFULL)) {
                                 ok = false;
                                 break;
                             }
                             if (k == 0 && epi > 0 &&
-                                !mbar_wait<INL>(bar(L::B_OEMPTY), (epi - 1) & 1, ctx, SITE_M_OEMPTY)) {
+                                !mbar_wait<INL, HN>(bar(L::B_OEMPTY), (epi - 1) & 1, ctx, SITE_M_OEMPTY)) {
                                 ok = false;
                                 break;
                             }
@@ -746,7 +747,7 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                 // S buffers take consecutive jobs in turn
                 const uint32_t b = NQ == 2 ? (uint32_t)t : (pv % L::NSB);
                 const uint32_t ph = NQ == 2 ? (pv & 1) : ((pv / L::NSB) & 1);
-                if (!mbar_wait_warp<INL, L1>(bar(L::B_SFULL + b), ph, ctx, SITE_S_SFULL)) {
+                if (!mbar_wait_warp<INL, L1, HN>(bar(L::B_SFULL + b), ph, ctx, SITE_S_SFULL)) {
                     ok = false;
                     break;
                 }
@@ -840,7 +841,7 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                 // them).  One tile: P goes over the first columns of this S buffer.
                 uint8_t *prow = smem + L::OFF_P + t * L::P_TILE + rit * 128;
                 if constexpr (F8) {   // measured faster with the wait ahead of the exponentials
-                    if (pv > 0 && !mbar_wait_warp<INL>(bar(L::B_ODONE + t), (pv - 1) & 1, ctx, SITE_S_ODONE)) {
+                    if (pv > 0 && !mbar_wait_warp<INL, false, HN>(bar(L::B_ODONE + t), (pv - 1) & 1, ctx, SITE_S_ODONE)) {
                         ok = false;
                         break;
                     }
@@ -877,7 +878,7 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                         tmem_st_x16(lane_base + L::S_COL + b * BC + c * 16, pk);
                 }
                 if constexpr (L::PSM) {
-                    if (!F8 && pv > 0 && !mbar_wait_warp<INL>(bar(L::B_ODONE + t), (pv - 1) & 1, ctx, SITE_S_ODONE)) {
+                    if (!F8 && pv > 0 && !mbar_wait_warp<INL, false, HN>(bar(L::B_ODONE + t), (pv - 1) & 1, ctx, SITE_S_ODONE)) {
                         ok = false;
                         break;
                     }
@@ -903,7 +904,7 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                     // O~ must hold the previous PV of this tile before it is rescaled (two tiles:
                     // waited for above)
                     if (!L::PSM &&
-                        !mbar_wait_warp<INL, L1>(bar(L::B_ODONE + ((pv - 1) & 1)), ((pv - 1) >> 1) & 1, ctx, SITE_S_ODONE)) {
+                        !mbar_wait_warp<INL, L1, HN>(bar(L::B_ODONE + ((pv - 1) & 1)), ((pv - 1) >> 1) & 1, ctx, SITE_S_ODONE)) {
                         ok = false;
                         break;
                     }
@@ -944,7 +945,7 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
             // epilogue: O = O~ / l, lse = c m + ln l.  With one tile the softmax can be up
             // to two PVs ahead of the tensor core here, too far for a parity wait on the
             // per-PV barrier; the per-unit barrier completes exactly once per epilogue.
-            if (!mbar_wait_warp<INL, L1>(bar(L::B_OFINAL + t), ep & 1, ctx, SITE_S_EPI))
+            if (!mbar_wait_warp<INL, L1, HN>(bar(L::B_OFINAL + t), ep & 1, ctx, SITE_S_EPI))
                 break;
             ++ep;
             tc_fence_after();
