@@ -60,27 +60,34 @@ def measured_peaks() -> dict:
         return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
 
 
-PROFILE_OF = {"bwd_main": ("profiles/bwd_main_d128_b2h32_t4096_causal.md", ("fa_bwd_sm103.cu", "fa_common.cuh")),
-              "fwd": ("profiles/fwd_kernel_d128_b2h32_t4096_causal.md", ("fa_fwd_sm103.cu", "fa_common.cuh"))}
+# Committed ncu summaries: (kernel, head width) -> (summary, the sources its hash covers).  A
+# summary lists, per full-size workload it was scaled to, "dram-bytes-per-launch-<key>: N".
+_FWD_SRC, _BWD_SRC = ("fa_fwd_sm103.cu", "fa_common.cuh"), ("fa_bwd_sm103.cu", "fa_common.cuh")
+PROFILE_OF = {("bwd_main", 128): ("profiles/bwd_main_d128_b2h32_t4096_causal.md", _BWD_SRC),
+              ("fwd", 128): ("profiles/fwd_kernel_d128_b2h32_t4096_causal.md", _FWD_SRC),
+              ("fwd", 256): ("profiles/fwd_kernel_d256_b1h4_t32768_causal.md", _FWD_SRC),
+              ("fwd", 64): ("profiles/fwd_kernel_d64_b1h6_t65536.md", _FWD_SRC),
+              ("bwd_main", 64): ("profiles/bwd_main_d64_b1h6_t65536.md", _BWD_SRC)}
 
 
-def ncu_traffic(kernel: str) -> int | None:
-    """DRAM bytes (read + write) per full-size launch from the committed ncu summary of
-    `kernel`, or None when the kernel's sources changed since that capture."""
+def ncu_traffic(kernel: str, d: int = 128, key: str = "b8h32") -> int | None:
+    """DRAM bytes (read + write) per full-size launch of workload `key` from the committed ncu
+    summary of `kernel` at head width d, or None: no such summary or figure, or the kernel's
+    sources changed since that capture."""
     import hashlib
     import re
-    path, srcs = PROFILE_OF[kernel]
+    if (kernel, d) not in PROFILE_OF:
+        return None
+    path, srcs = PROFILE_OF[(kernel, d)]
     try:
         text = open(os.path.join(ROOT, path)).read()
         h = hashlib.sha256()
         for f in srcs:
             h.update(open(os.path.join(ROOT, "exact_io_aware_05_gb300", "csrc", f), "rb").read())
-        sha = re.search(r"source-sha256-16:\s*([0-9a-f]{16})", text).group(1)
-        if sha != h.hexdigest()[:16]:
+        sha = re.search(r"source-sha256-16:\s*([0-9a-f]{16})", text)
+        if sha.group(1) != h.hexdigest()[:16]:
             return None
-        if WORKLOAD["B"] != 8:
-            return None
-        return int(re.search(r"dram-bytes-per-launch-b8h32:\s*(\d+)", text).group(1))
+        return int(re.search(rf"dram-bytes-per-launch-{re.escape(key)}:\s*(\d+)", text).group(1))
     except Exception:
         return None
 
@@ -399,7 +406,7 @@ def run_ours(args) -> None:
                    "bwd": {"ms": pre_ms + main_ms + dq_ms, "tflops": bwd_tf, "pct_of_peak": 100 * bwd_tf / peak,
                            "preprocess_ms": pre_ms, "tile_loop_ms": main_ms, "dq_finish_ms": dq_ms}},
         "roofline": {"kernel": dom[0], "bound": "tensor", "achieved": dom[1], "peak": peak, "unit": "TFLOP/s",
-                     "frac": dom[1] / peak, "traffic": ncu_traffic(dom[0]),
+                     "frac": dom[1] / peak, "traffic": ncu_traffic(dom[0]) if WORKLOAD["B"] == 8 else None,
                      "peak_source": f"{peaks['source']} bf16 (burst), MEASURED_PEAKS.json"},
         "gpu_launches": KERNELS_PER_STEP * args.steps,
         "e2e": e2e,
@@ -578,6 +585,8 @@ def run_config(args) -> None:
     stream = torch.cuda.current_stream(dev)
     for name in names:
         w = inputs.WORKLOADS[name]
+        if args.heads is not None:   # profiling size: fewer heads, same shape per head
+            w = inputs.replace(w, H=args.heads, name=f"{w.name} (profiling size: H{args.heads})")
         f32 = w.dtype == torch.float32
         g = torch.Generator(device=dev)
         g.manual_seed(4321 + w.seed)
@@ -668,7 +677,7 @@ def run_config(args) -> None:
             else:
                 dom = ("fwd", passes["fwd"]["tflops"])
             roof = {"kernel": dom[0], "bound": "tensor", "achieved": dom[1], "peak": peak, "unit": "TFLOP/s",
-                    "frac": dom[1] / peak, "traffic": None,
+                    "frac": dom[1] / peak, "traffic": ncu_traffic(dom[0], w.d, w.name) if args.heads is None else None,
                     "peak_source": f"{peaks['source']} bf16 (burst), MEASURED_PEAKS.json"}
         # end to end: the same calls with the inputs copied in from pinned host memory and the
         # outputs copied back, all inside the timed region
@@ -751,6 +760,8 @@ def main():
                     help="time configured workload 1..5 (each variant) instead of the headline step")
     ap.add_argument("--batch", type=int, default=WORKLOAD["B"],
                     help="batch size (default 8, the benchmark workload; smaller only for profiling)")
+    ap.add_argument("--heads", type=int, default=None,
+                    help="with --config: heads per workload (default: the workload's; fewer only for profiling)")
     args = ap.parse_args()
     if args.batch != WORKLOAD["B"]:
         WORKLOAD["B"] = args.batch
