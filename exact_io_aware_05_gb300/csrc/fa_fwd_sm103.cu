@@ -25,7 +25,8 @@
 //   * warps 1 and 2 (two tiles): one thread each issues the tcgen05.mma and
 //     commits of its tile, S of key block k+1 ahead of P V of block k (P lives
 //     in shared memory, so S may be overwritten once the softmax has read it);
-//     with one tile, warp 1 issues the S products and warp 2 the P V products;
+//     with one tile, warp 1 issues the S products and warp 2 the P V products,
+//     and the K/V ring holds 16 KB chunks that each product consumes in order;
 //   * one 128-thread softmax warpgroup per query tile (thread = query row =
 //     tensor-memory lane) doing the online softmax and the epilogue; the two
 //     warpgroups run independently;
@@ -55,15 +56,15 @@ template <int D>
 struct FwdCfg;
 template <>
 struct FwdCfg<64> {
-    static constexpr int BC = 128, NQ = 2, NSLOT = 8;
+    static constexpr int BC = 128, NQ = 2;
 };
 template <>
 struct FwdCfg<128> {
-    static constexpr int BC = 128, NQ = 2, NSLOT = 4;
+    static constexpr int BC = 128, NQ = 2;
 };
 template <>
 struct FwdCfg<256> {
-    static constexpr int BC = 64, NQ = 1, NSLOT = 4;
+    static constexpr int BC = 128, NQ = 1;
 };
 
 // F8: e4m3 operands (Q, K row-major; V transposed, [channel][key]), d = 128 only.
@@ -94,15 +95,24 @@ struct FwdLayout {
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_P = NQ * Q_TILE;
     static constexpr int OFF_SLOT = OFF_P + NQ * P_TILE;
-    // K/V ring: as many slots as the remaining shared memory holds, at most 8
-    static constexpr int NSLOT_FIT = (227 * 1024 - 1024 - 512 - OFF_SLOT) / KV_TILE;
-    static constexpr int NSLOT = PSM ? (NSLOT_FIT < 8 ? NSLOT_FIT : 8) : (F8 ? 8 : C::NSLOT);
-    static_assert(NSLOT >= 3, "K/V ring depth");
-    static constexpr int OFF_BAR = OFF_SLOT + NSLOT * KV_TILE;
-    // S buffers in tensor memory: one per tile with two tiles; with one tile, three that
-    // the key blocks take in turn (P goes back over S there, so S of block k + 3 waits
-    // only for P V of block k)
-    static constexpr int NSB = NQ == 1 ? 3 : 2;
+    // K/V ring.  Two tiles: a slot holds a whole K_j or V_j tile.  One tile (d = 256): a slot
+    // holds a 16 KB chunk, so that a 64 KB tile streams through the ring and each chunk is
+    // released as soon as its products have read it: K_j in KCH chunks of 64 channels (S
+    // consumes them in order along its contraction), V_j in VCH chunks of 32 keys, each
+    // [KCH][32 keys][128 bytes] (P V consumes them in order along its contraction).
+    static constexpr int VCH = BC / 32;
+    static_assert(NQ != 1 || (VCH == KCH && VCH * 32 * 128 * KCH == KCH * KV_CHUNK), "one tile: equal chunks");
+    static constexpr int SLOT_BYTES = NQ == 1 ? KV_CHUNK : KV_TILE;
+    // as many slots as the remaining shared memory holds, at most 8 (one tile: 12 chunks)
+    static constexpr int NSLOT_FIT = (227 * 1024 - 1024 - 512 - OFF_SLOT) / SLOT_BYTES;
+    static constexpr int NSLOT = PSM ? (NSLOT_FIT < 8 ? NSLOT_FIT : 8)
+                                     : (F8 ? 8 : (NSLOT_FIT < 12 ? NSLOT_FIT : 12));
+    static_assert(NSLOT >= 3 && (NQ != 1 || NSLOT >= 2 * KCH + 1), "K/V ring depth");
+    static constexpr int OFF_BAR = OFF_SLOT + NSLOT * SLOT_BYTES;
+    // S buffers in tensor memory: one per tile with two tiles; with one tile two that the
+    // key blocks take in turn (P goes back over S there, so S of block k + 2 waits for P V
+    // of block k)
+    static constexpr int NSB = 2;
     // barrier indices
     static constexpr int B_FULL = 0, B_EMPTY = NSLOT, B_QFULL = 2 * NSLOT, B_QEMPTY = 2 * NSLOT + 1,
                          B_SFULL = 2 * NSLOT + 2, B_PFULL = B_SFULL + NSB, B_ODONE = B_PFULL + NSB,
@@ -438,6 +448,25 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                         ++n_loads;
                         return true;
                     };
+                    // one tile: K_j or V_j as KCH chunk slots (see FwdLayout)
+                    auto load_chunks = [&](bool is_k, int j) -> bool {
+                        for (int c = 0; c < L::KCH; ++c) {
+                            const uint32_t slot = n_loads % NSLOT;
+                            if (n_loads >= NSLOT &&
+                                !mbar_wait<INL, HN>(bar(L::B_EMPTY + slot), ((n_loads / NSLOT) - 1) & 1, ctx, SITE_P_EMPTY))
+                                return false;
+                            mbar_arrive_expect_tx(bar(L::B_FULL + slot), L::SLOT_BYTES);
+                            const uint32_t dst = sbase + L::OFF_SLOT + slot * L::SLOT_BYTES;
+                            if (is_k)   // channels [64c, 64c + 64) of the block's BC keys
+                                tma_load_3d_hint(dst, &tm_k, bar(L::B_FULL + slot), c * L::CH_ELEMS, j * BC, p.bh, pol_kv);
+                            else        // keys [32c, 32c + 32), all channels, 64 at a time
+                                for (int dc = 0; dc < L::KCH; ++dc)
+                                    tma_load_3d_hint(dst + dc * 32 * 128, &tm_v, bar(L::B_FULL + slot), dc * L::CH_ELEMS,
+                                                     j * BC + 32 * c, p.bh, pol_kv);
+                            ++n_loads;
+                        }
+                        return true;
+                    };
                     bool ok = true;
                     if constexpr (NQ == 2) {
                         // each tile's MMA warp consumes K_j, V_j of every block either tile visits,
@@ -461,12 +490,12 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                         ok = walk_ops(
                             p.J,
                             [&](int) {
-                                const bool r = load(&tm_k, kj);
+                                const bool r = load_chunks(true, kj);
                                 kj = next_active<BC>(p.tr0, kj + 1);
                                 return r;
                             },
                             [&](int) {
-                                const bool r = load(&tm_v, vj);
+                                const bool r = load_chunks(false, vj);
                                 vj = next_active<BC>(p.tr0, vj + 1);
                                 return r;
                             });
@@ -615,13 +644,15 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
             // the S buffer that it overwrites, and P V(k) as soon as the softmax has written
             // P(k).  A tcgen05.mma blocks its issuing thread while the tensor core's queue is
             // full, so with one issuer every wait of one product stalled the other's issue.
-            // Both warps locate their tiles in the K/V ring by the producer's load order of the
-            // unit, S(0), S(1), PV(0), S(2), PV(1), ...: S(k) is load k ? 2k - 1 : 0 and P V(k)
-            // is load min(J, k + 2) + k.
+            // Both warps locate their chunks in the K/V ring by the producer's load order of the
+            // unit, S(0), S(1), PV(0), S(2), PV(1), ..., KCH chunks each: S(k) is op k ? 2k - 1 : 0
+            // and P V(k) is op min(J, k + 2) + k.  Each chunk is released as soon as the
+            // products that read it have completed.
             if (lane == 0) {
                 const bool s_side = warp == 1;
                 uint32_t base = 0, kg = 0, q_seen = 0, epi = 0;
                 bool ok = true;
+                const uint64_t qd = sdesc_sw128(sbase + L::OFF_Q, 16, 1024);
                 for (int pass = 0, u = snake_unit<!MASKED>(0); u < a.units && ok; u = snake_unit<!MASKED>(++pass)) {
                     const Plan p = make_plan<D, MASKED>(u, a);
                     const int J = p.J;
@@ -634,12 +665,8 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                     }
                     for (int k = 0; k < J && ok; ++k) {
                         const uint32_t g = kg + k, b = g % L::NSB;
-                        const uint32_t n = base + (uint32_t)(s_side ? (k ? 2 * k - 1 : 0) : min(J, k + 2) + k);
-                        const uint32_t slot = n % NSLOT;
-                        if (!mbar_wait<INL, HN>(bar(L::B_FULL + slot), (n / NSLOT) & 1, ctx, SITE_M_FULL)) {
-                            ok = false;
-                            break;
-                        }
+                        const uint32_t op = (uint32_t)(s_side ? (k ? 2 * k - 1 : 0) : min(J, k + 2) + k);
+                        const uint32_t n0 = base + op * L::KCH;   // first chunk of this product
                         if (s_side) {
                             // S(g) overwrites the columns that held P(g - NSB): P V(g - NSB) must
                             // have finished reading them
@@ -648,17 +675,27 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                                 ok = false;
                                 break;
                             }
-                            tc_fence_after();
-                            const uint64_t qd = sdesc_sw128(sbase + L::OFF_Q, 16, 1024);
-                            const uint64_t kd = sdesc_sw128(sbase + L::OFF_SLOT + slot * L::KV_TILE, 16, 1024);
+                            // K_j chunk c: channels [64c, 64c + 64), four K steps of 16
 #pragma unroll
-                            for (int kk = 0; kk < D / 16; ++kk) {   // 16 bf16 = 32 bytes along K
-                                const uint32_t off = ((kk >> 2) * L::Q_CHUNK + (kk & 3) * 32) >> 4;
-                                const uint32_t offk = ((kk >> 2) * L::KV_CHUNK + (kk & 3) * 32) >> 4;
-                                mma_ss(tmem + L::S_COL + b * BC, qd + off, kd + offk, L::IDESC_S, kk > 0 ? 1u : 0u);
+                            for (int c = 0; c < L::KCH; ++c) {
+                                const uint32_t n = n0 + c, slot = n % NSLOT;
+                                if (!mbar_wait<INL, HN>(bar(L::B_FULL + slot), (n / NSLOT) & 1, ctx, SITE_M_FULL)) {
+                                    ok = false;
+                                    break;
+                                }
+                                tc_fence_after();
+                                const uint64_t kd = sdesc_sw128(sbase + L::OFF_SLOT + slot * L::SLOT_BYTES, 16, 1024);
+#pragma unroll
+                                for (int kk = 0; kk < 4; ++kk) {   // 16 bf16 = 32 bytes along K
+                                    const uint32_t off = (c * L::Q_CHUNK + kk * 32) >> 4;
+                                    mma_ss(tmem + L::S_COL + b * BC, qd + off, kd + ((kk * 32) >> 4), L::IDESC_S,
+                                           (c > 0 || kk > 0) ? 1u : 0u);
+                                }
+                                tc_commit(bar(L::B_EMPTY + slot));
                             }
+                            if (!ok)
+                                break;
                             tc_commit(bar(L::B_SFULL + b));
-                            tc_commit(bar(L::B_EMPTY + slot));
                             if (k == J - 1)
                                 tc_commit(bar(L::B_QEMPTY));
                         } else {
@@ -671,31 +708,36 @@ __global__ void __launch_bounds__(FwdLayout<D, F8>::NTHREADS, 1)
                                 ok = false;
                                 break;
                             }
-                            tc_fence_after();
-                            const uint64_t vd = sdesc_sw128(sbase + L::OFF_SLOT + slot * L::KV_TILE, L::KV_CHUNK, 1024);
-                            if (k == 0) {
+                            // V_j chunk c: keys [32c, 32c + 32) as [KCH][32 keys][128 bytes], two K
+                            // steps of 16 keys; P from tensor memory (16 keys = 8 packed columns)
 #pragma unroll
-                                for (int kk = 0; kk < BC / 16; ++kk)
-                                    mma_ts(tmem + L::O_COL, tmem + L::S_COL + b * BC + kk * 8,
-                                           vd + ((kk * 16 * 128) >> 4), L::IDESC_PV, kk > 0 ? 1u : 0u);
-                            } else {
+                            for (int c = 0; c < L::VCH; ++c) {
+                                const uint32_t n = n0 + c, slot = n % NSLOT;
+                                if (!mbar_wait<INL, HN>(bar(L::B_FULL + slot), (n / NSLOT) & 1, ctx, SITE_M_FULL)) {
+                                    ok = false;
+                                    break;
+                                }
+                                tc_fence_after();
+                                const uint64_t vd = sdesc_sw128(sbase + L::OFF_SLOT + slot * L::SLOT_BYTES, 32 * 128, 1024);
 #pragma unroll
-                                for (int kk = 0; kk < BC / 16; ++kk)
-                                    mma_ts(tmem + L::O_COL, tmem + L::S_COL + b * BC + kk * 8,
-                                           vd + ((kk * 16 * 128) >> 4), L::IDESC_PV, 1u);
+                                for (int kk = 0; kk < 2; ++kk)
+                                    mma_ts(tmem + L::O_COL, tmem + L::S_COL + b * BC + (2 * c + kk) * 8,
+                                           vd + ((kk * 16 * 128) >> 4), L::IDESC_PV, (k > 0 || c > 0 || kk > 0) ? 1u : 0u);
+                                tc_commit(bar(L::B_EMPTY + slot));
                             }
+                            if (!ok)
+                                break;
                             // O~ holds P V(g): the softmax may be up to NSB jobs ahead, so the
                             // signal alternates between two barriers to stay within one phase
                             tc_commit(bar(L::B_ODONE + (g & 1)));
                             tc_commit(bar(L::B_PREAD + b));
-                            tc_commit(bar(L::B_EMPTY + slot));
                             if (k == J - 1) {   // last P V of the unit
                                 tc_commit(bar(L::B_OFINAL));
                                 ++epi;
                             }
                         }
                     }
-                    base += 2u * (uint32_t)J;
+                    base += 2u * (uint32_t)L::KCH * (uint32_t)J;
                     kg += (uint32_t)J;
                 }
                 // drain: all MMAs this thread issued complete before tensor memory is released
@@ -1003,7 +1045,7 @@ int launch(const void *q, const void *k, const void *v, void *o, float *lse, int
     if (st == OK)
         st = encode_tmap_3d(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, Tk, BH, 64, L::BC);
     if (st == OK)
-        st = encode_tmap_3d(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, Tk, BH, 64, L::BC);
+        st = encode_tmap_3d(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, Tk, BH, 64, L::NQ == 1 ? 32 : L::BC);
     if (st != OK)
         return st;
     FwdArgs a;
