@@ -84,6 +84,10 @@ SMALL = [
     (1, 2, 330, 190, 256, False), (1, 2, 200, 700, 128, True), (1, 2, 700, 200, 128, True),
     (1, 2, 700, 200, 64, True), (1, 1, 1, 1, 128, False), (1, 1, 5, 3, 64, True), (1, 1, 129, 257, 256, True),
     (3, 1, 1000, 1000, 64, True),
+    # d = 256 streams K and V through 16 KB chunks (64 channels of K, 32 keys of V): key counts
+    # that end inside, or before, a chunk
+    (1, 1, 3, 5, 256, True), (1, 2, 64, 33, 256, False), (1, 1, 200, 1, 256, False),
+    (2, 3, 140, 420, 256, True), (1, 1, 1, 160, 256, False),
 ]
 
 
